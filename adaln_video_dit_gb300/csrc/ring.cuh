@@ -1,0 +1,160 @@
+// Shared-memory staging ring used by the forward and backward row kernels.
+//
+// A CTA = nc consumer warps + 1 producer warp.  The producer (one lane)
+// streams chunks of R consecutive rows from global memory into S ring stages
+// with bulk asynchronous copies, each completing on the stage's "full"
+// mbarrier; consumer warps release a stage on its "empty" mbarrier as soon as
+// they have moved its contents into registers.  Consumer thread j owns the
+// 16-byte column vectors j, j + 32 nc, ... of every row, so column state
+// (modulation vectors, gradient accumulators) stays in its registers for the
+// whole row range, and row sums are finished with a warp butterfly plus one
+// exchange through shared memory per round of R rows.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace adaln {
+
+struct Ring {
+  uint32_t base;   // shared address of the dynamic shared memory
+  int stages;
+  volatile int* abort;
+  float* red;      // [2][kMaxConsumerWarps][R][2]
+  int* okf;        // [2][kMaxConsumerWarps]
+  unsigned char* ring;
+
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (stages + s); }
+};
+
+__device__ __forceinline__ Ring ring_layout(unsigned char* smem, int stages) {
+  Ring r;
+  r.base = smem_addr(smem);
+  r.stages = stages;
+  unsigned char* p = smem + 16 * stages;
+  r.abort = reinterpret_cast<volatile int*>(p);
+  p += 16;
+  r.red = reinterpret_cast<float*>(p);
+  p += 2 * kMaxConsumerWarps * kRowsPerRound * 2 * 4;
+  r.okf = reinterpret_cast<int*>(p);
+  r.ring = smem + ring_header_bytes(stages);
+  return r;
+}
+
+// Thread 0 initialises the barriers; everyone syncs.  Must run before the
+// role split (it uses __syncthreads).
+__device__ __forceinline__ void ring_init(const Ring& rg, int nc) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < rg.stages; ++s) {
+      mbar_init(rg.full(s), 1);
+      mbar_init(rg.empty(s), nc);
+    }
+    *rg.abort = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+}
+
+// Producer loop (one lane).  Streams `nchunks` chunks of up to R rows of each
+// of NT tensors (src[i] + row offset) into the ring.  Before returning it
+// waits for the last copy issued into every stage, so that no copy into this
+// CTA's shared memory is still in flight when the CTA exits.
+template <int R, int NT>
+__device__ __forceinline__ void ring_produce(const Ring& rg,
+                                             const unsigned char* const (&src)[NT],
+                                             int64_t nrows, int row_bytes,
+                                             unsigned* status) {
+  const uint64_t policy = l2_evict_first_policy();
+  const int64_t nchunks = (nrows + R - 1) / R;
+  const int S = rg.stages;
+  const uint32_t stage_bytes = (uint32_t)R * row_bytes * NT;
+  int64_t issued = 0;
+  for (int64_t k = 0; k < nchunks; ++k) {
+    const int s = (int)(k % S);
+    const int64_t it = k / S;
+    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (uint32_t)((it - 1) & 1), rg.abort)) {
+      if (!*rg.abort) atomicOr(status, ADALN_DEV_TIMEOUT);
+      *rg.abort = 1;
+      break;
+    }
+    if (*rg.abort) break;
+    const int rows = (int)min((int64_t)R, nrows - k * R);
+    const uint32_t bytes = (uint32_t)rows * row_bytes;
+    mbar_arrive_expect_tx(rg.full(s), bytes * NT);
+    const uint32_t dst = smem_addr(rg.ring) + (uint32_t)s * stage_bytes;
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+      bulk_g2s(dst + (uint32_t)i * R * row_bytes,
+               src[i] + (size_t)k * R * row_bytes, bytes, rg.full(s), policy);
+    issued = k + 1;
+  }
+  // Drain: the newest chunk of each stage is the only one possibly in flight.
+  for (int s = 0; s < S; ++s) {
+    if (issued <= s) break;
+    const int64_t last = s + ((issued - 1 - s) / S) * S;
+    if (!mbar_wait_bounded(rg.full(s), (uint32_t)((last / S) & 1), nullptr))
+      atomicOr(status, ADALN_DEV_TIMEOUT);
+  }
+}
+
+// Sum K values per row over the consumer team, for R rows at once.  Every
+// consumer thread gets bitwise identical sums (butterflies of commutative
+// adds, fixed shape).  `ok` is this thread's pipeline status; the returned
+// flag is true only if every consumer warp was ok, so all consumers take the
+// same branch after the exchange.  `phase` alternates the shared buffers.
+template <int R, int K>
+__device__ __forceinline__ bool team_sum(float (&v)[R][K], bool ok,
+                                         const Ring& rg, int nc, int phase) {
+  static_assert(R <= kRowsPerRound && K <= 2, "reduction buffer too small");
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      float a = v[r][q];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      v[r][q] = a;
+    }
+  const bool warp_ok = __all_sync(0xffffffffu, ok);
+  float* red = rg.red + phase * (kMaxConsumerWarps * kRowsPerRound * 2);
+  int* okf = rg.okf + phase * kMaxConsumerWarps;
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int q = 0; q < K; ++q) red[(w * kRowsPerRound + r) * 2 + q] = v[r][q];
+    okf[w] = warp_ok ? 1 : 0;
+  }
+  named_barrier_sync(1, nc * 32);
+  const bool mine = lane < nc;
+  bool all_ok = __all_sync(0xffffffffu, mine ? okf[lane] != 0 : true);
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      float a = mine ? red[(lane * kRowsPerRound + r) * 2 + q] : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      v[r][q] = a;
+    }
+  return all_ok;
+}
+
+// Read a row's segment id, clamp it into [0, nseg) and record range / order
+// violations (thread 0 of the CTA only reports).
+__device__ __forceinline__ int checked_seg(int raw, int prev, int nseg,
+                                           unsigned* status) {
+  int b = raw;
+  unsigned bad = 0;
+  if (b < 0 || b >= nseg) {
+    bad |= ADALN_DEV_SEG_RANGE;
+    b = b < 0 ? 0 : nseg - 1;
+  }
+  if (b < prev) bad |= ADALN_DEV_SEG_ORDER;
+  if (bad && threadIdx.x == 0) atomicOr(status, bad);
+  return b;
+}
+
+}  // namespace adaln

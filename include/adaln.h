@@ -1,0 +1,170 @@
+/*
+ * libadaln -- fused AdaLN LayerNorm-Modulate for GB300 (sm_103a).
+ *
+ * The operator is the fused adaptive LayerNorm of video / MMDiT diffusion
+ * transformers described in "AdaptiveLoad: Towards Efficient Video Diffusion
+ * Transformer Training", Technical summary, section 2.B ("Fused
+ * LayerNorm-Modulate CUDA kernels"): normalisation and modulation in a single
+ * kernel launch (forward), and a backward whose modulation-gradient reduction
+ * along the sequence dimension is laid out so that each thread owns a feature
+ * column d and accumulates down the sequence (the "D-tile coalesced
+ * reduction").  The pages give no formula; this library computes, for every
+ * token row t of a packed variable-length batch with b = seg_id[t]:
+ *
+ *   mean[t] = (1/D) sum_d x[t,d]
+ *   var[t]  = (1/D) sum_d (x[t,d] - mean[t])^2         (biased)
+ *   rstd[t] = 1 / sqrt(var[t] + eps)
+ *   xhat    = (x - mean[t]) * rstd[t]
+ *   y       = xhat * (1 + scale[b,d]) + shift[b,d]
+ *   g       = dy * (1 + scale[b,d])
+ *   dx      = rstd[t] * (g - mean_d(g) - xhat * mean_d(g * xhat))
+ *   dscale[b,d] = sum_{t: seg_id[t]=b} dy[t,d] * xhat[t,d]
+ *   dshift[b,d] = sum_{t: seg_id[t]=b} dy[t,d]
+ *
+ * Layout: all tensors row-major and contiguous.  x, y, dy, dx are [T, D];
+ * shift, scale are [nseg, D]; all of these have the element type `dtype`.
+ * seg_id is int32 [T]; mean, rstd are fp32 [T]; dshift, dscale are fp32
+ * [nseg, D].  Arithmetic is fp32; bf16 outputs are rounded once (to nearest
+ * even) at the store.
+ *
+ * Ownership: every pointer is owned by the caller and must point to device
+ * memory of the current CUDA device (except host_* arguments).  The library
+ * never allocates, frees or retains caller memory.
+ *
+ * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) and the calls return without synchronising.  Return codes
+ * report errors detectable on the host before launch, and launch failures.
+ * Data errors found on the device (a seg_id outside [0, nseg) or decreasing
+ * along the rows) are clamped so that every access stays in bounds, and are
+ * recorded in a per-device status word read by adaln_get_status(); outputs of
+ * such a call are unspecified.
+ *
+ * Preconditions (checked, ADALN_ERR_* on violation):
+ *   - T >= 0 (T = 0 does nothing, except that adaln_bwd zeroes dshift/dscale);
+ *   - D >= 1, D * sizeof(element) a multiple of 16 bytes (D % 8 == 0 for bf16,
+ *     D % 4 == 0 for fp32), D <= ADALN_MAX_D_BF16 / ADALN_MAX_D_F32;
+ *   - 1 <= nseg <= ADALN_MAX_NSEG;
+ *   - x, y, dy, dx, shift, scale, dshift, dscale and the workspace 16-byte
+ *     aligned; seg_id, mean, rstd 4-byte aligned;
+ *   - eps finite and >= 0;
+ *   - seg_id non-decreasing along rows (segments packed contiguously), values
+ *     in [0, nseg).  Segments may be empty.
+ */
+#ifndef ADALN_H
+#define ADALN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbol visibility of the exported entry points. */
+#if defined(__GNUC__)
+#define ADALN_API __attribute__((visibility("default")))
+#else
+#define ADALN_API
+#endif
+
+#define ADALN_MAX_D_BF16 8192
+#define ADALN_MAX_D_F32 4096
+#define ADALN_MAX_NSEG (1 << 24)
+
+typedef enum {
+  ADALN_F32 = 0,  /* IEEE binary32 */
+  ADALN_BF16 = 1  /* bfloat16 */
+} adaln_dtype_t;
+
+typedef enum {
+  ADALN_OK = 0,
+  ADALN_ERR_NULL = 1,      /* a required pointer is NULL */
+  ADALN_ERR_DIM = 2,       /* T, D or nseg outside the supported range */
+  ADALN_ERR_ALIGN = 3,     /* a pointer is not aligned as required */
+  ADALN_ERR_DTYPE = 4,     /* unknown dtype */
+  ADALN_ERR_SEG = 5,       /* device status: seg_id out of range or decreasing */
+  ADALN_ERR_WORKSPACE = 6, /* workspace NULL or smaller than required */
+  ADALN_ERR_CUDA = 7,      /* a CUDA runtime call or launch failed */
+  ADALN_ERR_ARG = 8,       /* eps negative or not finite; bad trace argument */
+  ADALN_ERR_TIMEOUT = 9    /* device status: an internal pipeline wait gave up */
+} adaln_status_t;
+
+/* Bits of the device status word (adaln_get_status). */
+#define ADALN_DEV_SEG_RANGE 1u   /* a seg_id was outside [0, nseg) */
+#define ADALN_DEV_SEG_ORDER 2u   /* seg_id decreased from one row to the next */
+#define ADALN_DEV_TIMEOUT 4u     /* a bounded wait on a copy pipeline expired */
+
+/*
+ * Forward (section 2.B, forward pass): per-row statistics reduced on chip and
+ * the modulation applied in the same launch.  Reads x once, writes y, mean,
+ * rstd.  One kernel launch on `stream`.
+ */
+ADALN_API int adaln_fwd(const void* x, const void* shift, const void* scale,
+              const int32_t* seg_id, int64_t T, int32_t D, int32_t nseg,
+              adaln_dtype_t dtype, float eps, void* y, float* mean,
+              float* rstd, void* stream);
+
+/*
+ * Bytes of device workspace adaln_bwd needs for these sizes on the current
+ * device (it depends on the device's SM count).  Written to *bytes.
+ */
+ADALN_API int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg,
+                             adaln_dtype_t dtype, size_t* bytes);
+
+/*
+ * Backward (section 2.B, backward pass with the D-tile coalesced reduction).
+ * Reads dy and x once (plus the saved mean/rstd), writes dx [T, D] and the
+ * fp32 sequence reductions dshift, dscale [nseg, D].  Two kernel launches on
+ * `stream`: a row pass that also accumulates per-(CTA, segment) column
+ * partials into `workspace`, then a fixed-order reduction of those partials.
+ * No floating-point atomics: for a given device and sizes the results are
+ * bitwise reproducible.  `workspace` (>= adaln_bwd_workspace_size bytes,
+ * 16-byte aligned) is scratch owned by the caller; its contents on entry do
+ * not matter.  Calls sharing one workspace must not overlap on the device.
+ */
+ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
+              const float* rstd, const void* scale, const int32_t* seg_id,
+              int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype,
+              void* dx, float* dshift, float* dscale, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * *host_bits (if non-NULL) receives the ADALN_DEV_* bits.  Returns ADALN_OK,
+ * ADALN_ERR_SEG, ADALN_ERR_TIMEOUT or ADALN_ERR_CUDA.  The word is shared by
+ * all calls on the device since it was last cleared.
+ */
+ADALN_API int adaln_get_status(uint32_t* host_bits, void* stream);
+
+/* Static description of a status code. */
+ADALN_API const char* adaln_strerror(int code);
+
+/*
+ * Kernel timing trace.  Between adaln_trace_begin(capacity) and
+ * adaln_trace_end(), every kernel launch made by this library (from any
+ * thread) is bracketed by a pair of CUDA events recorded on its stream, up to
+ * `capacity` launches.  adaln_trace_end() synchronises those events and sums
+ * the elapsed time per kernel; adaln_trace_get() reads the sums.
+ * Kernel ids: ADALN_KERNEL_FWD, ADALN_KERNEL_BWD_ROWS, ADALN_KERNEL_BWD_FINALIZE.
+ */
+#define ADALN_KERNEL_FWD 0
+#define ADALN_KERNEL_BWD_ROWS 1
+#define ADALN_KERNEL_BWD_FINALIZE 2
+#define ADALN_NUM_KERNELS 3
+ADALN_API int adaln_trace_begin(int capacity);
+ADALN_API int adaln_trace_end(void);
+ADALN_API int adaln_trace_get(int kernel_id, int64_t* launches, double* total_ms);
+
+/*
+ * Launch shape chosen for these sizes on the current device: grid (CTAs),
+ * threads per CTA, ring stages, dynamic shared memory bytes.  `which` is
+ * ADALN_KERNEL_FWD or ADALN_KERNEL_BWD_ROWS.  For reports and tests.
+ */
+ADALN_API int adaln_launch_shape(int which, int64_t T, int32_t D, int32_t nseg,
+                       adaln_dtype_t dtype, int32_t* grid, int32_t* threads,
+                       int32_t* stages, int32_t* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ADALN_H */

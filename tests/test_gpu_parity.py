@@ -1,0 +1,231 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Workloads 1-2 are compared on every element; workloads 3-5 (full size, in the
+launch configuration the benchmark uses) on rows sampled at every CTA range
+boundary plus random rows, and on all of dscale/dshift.  Edge cases: empty
+input, single rows, T below the grid size, ragged tails, minimum and maximum
+D, every vectors-per-thread variant, empty and one-row segments, many
+segments.  Segment indexing is checked bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as H
+from adaln_video_dit_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status(adaln):
+    adaln.adaln_get_status()  # clear
+    yield
+    H.status_ok()
+
+
+@pytest.mark.parametrize("config", [1, 2])
+def test_workload_full_parity(adaln, config):
+    c = I.make(config)
+    d = H.device_inputs(c)
+    out = H.run_gpu(d, c["eps"])
+    H.check_against_oracle(c, d, out)
+
+
+@pytest.mark.parametrize("config", [3, 4])
+def test_workload_full_size_sampled_parity(adaln, config):
+    c = I.make(config)
+    d = H.device_inputs(c)
+    out = H.run_gpu(d, c["eps"])
+    grid = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, c["T"], c["D"], c["nseg"],
+                                    adaln.ADALN_BF16)["grid"]
+    rows = H.sample_rows(c["T"], grid)
+    H.check_against_oracle(c, d, out, rows=rows)
+
+
+def test_mmdit_joint_sites(adaln):
+    c = I.make(5, sites=3)
+    x, dy, seg = H.to_dev(c["x"]), H.to_dev(c["dy"]), H.to_dev(c["seg_id"])
+    rows = H.sample_rows(c["T"], 152, n_random=256)
+    for site in (0, 2):
+        d = dict(x=x, dy=dy, seg_id=seg, shift=H.to_dev(c["shift"][site]),
+                 scale=H.to_dev(c["scale"][site]), shift_np=c["shift"][site],
+                 scale_np=c["scale"][site])
+        out = H.run_gpu(d, c["eps"])
+        H.check_against_oracle(c, d, out, rows=rows)
+
+
+EDGE = [
+    # (T, D, nseg, dtype, lengths)
+    (1, 64, 1, "bf16", None),
+    (1, 4, 1, "f32", None),
+    (7, 8, 3, "bf16", [0, 7, 0]),          # T below the grid; empty first/last segment
+    (1001, 136, 5, "bf16", None),          # ragged: odd T, nvec = 17
+    (999, 24, 4, "f32", [1, 1, 1, 996]),   # one-row segments, nvec = 6
+    (300, 4096, 2, "bf16", None),          # nvec 512: VPT 1, 16 consumer warps
+    (300, 4104, 2, "bf16", None),          # nvec 513: VPT 2
+    (260, 6144, 3, "bf16", None),          # nvec 768: VPT 2, 12 consumer warps
+    (260, 6152, 3, "bf16", None),          # nvec 769: VPT 4
+    (200, 8192, 2, "bf16", None),          # largest bf16 row
+    (200, 4096, 2, "f32", None),           # largest fp32 row
+    (200, 2056, 2, "f32", None),           # fp32 nvec 514: VPT 2
+    (2048, 1536, 2048, "bf16", [1] * 2048),  # every row its own segment
+    (3000, 256, 700, "bf16", None),        # many segments, many empty
+]
+
+
+@pytest.mark.parametrize("T,D,nseg,dtype,lengths", EDGE,
+                         ids=[f"T{e[0]}_D{e[1]}_n{e[2]}_{e[3]}" for e in EDGE])
+def test_edge_shapes(adaln, T, D, nseg, dtype, lengths):
+    c = I.random_case(T * 31 + D, T, D, nseg, dtype=dtype, lengths=lengths, dy_std=1.0)
+    d = H.device_inputs(c)
+    out = H.run_gpu(d, c["eps"])
+    H.check_against_oracle(c, d, out)
+
+
+def test_empty_input_zeroes_modulation_grads(adaln):
+    dev = "cuda"
+    x = torch.empty(0, 64, device=dev, dtype=torch.bfloat16)
+    sh = torch.zeros(3, 64, device=dev, dtype=torch.bfloat16)
+    seg = torch.empty(0, device=dev, dtype=torch.int32)
+    y, m, r = adaln.adaln_fwd(x, sh, sh, seg, 1e-6)
+    assert y.shape == (0, 64)
+    dsh = torch.full((3, 64), float("nan"), device=dev)
+    dsc = torch.full((3, 64), float("nan"), device=dev)
+    adaln.adaln_bwd(x, x, m, r, sh, seg, dshift=dsh, dscale=dsc)
+    torch.cuda.synchronize()
+    assert torch.all(dsh == 0) and torch.all(dsc == 0)
+
+
+def test_segment_indexing_bit_exact(adaln):
+    """Constant rows give xhat = 0 exactly, so y = shift[seg_id] bit for bit;
+    with dy = 1, dshift[b] is exactly the segment length."""
+    lengths = [5, 0, 130, 1, 64, 0, 300, 12]
+    nseg, T, D = len(lengths), sum(lengths), 64
+    seg = I.seg_ids_from_lengths(lengths)
+    dev = "cuda"
+    for tdt in (torch.bfloat16, torch.float32):
+        x = torch.full((T, D), 0.5, device=dev, dtype=tdt)
+        scale = torch.zeros(nseg, D, device=dev, dtype=tdt)
+        shift = (torch.arange(nseg, device=dev, dtype=torch.float32) + 1)[:, None].expand(nseg, D)
+        shift = shift.contiguous().to(tdt)
+        segd = torch.from_numpy(seg).to(dev)
+        y, m, r = adaln.adaln_fwd(x, shift, scale, segd, 1e-6)
+        want = torch.from_numpy(seg.astype(np.float32) + 1).to(dev)[:, None].expand(T, D).to(tdt)
+        assert torch.equal(y, want)
+        dy = torch.ones(T, D, device=dev, dtype=tdt)
+        dx, dsh, dsc = adaln.adaln_bwd(dy, x, m, r, scale, segd)
+        want_sh = torch.tensor(lengths, device=dev, dtype=torch.float32)[:, None].expand(nseg, D)
+        assert torch.equal(dsh, want_sh)
+        assert torch.equal(dsc, torch.zeros_like(dsc))
+
+
+def _guarded(shape, dtype, fill, dev="cuda", pad=4096):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), fill, device=dev, dtype=dtype)
+    return buf, buf[pad:pad + n].view(*shape), pad
+
+
+def test_guard_bands_untouched(adaln):
+    """Outputs and workspace sit inside canary-filled buffers; nothing outside
+    the stated extents is written."""
+    c = I.random_case(77, 777, 1040, 9, dtype="bf16")
+    d = H.device_inputs(c)
+    T, D, nseg = c["T"], c["D"], c["nseg"]
+    bufs = {}
+    bufs["y"] = _guarded((T, D), torch.bfloat16, 7.0)
+    bufs["dx"] = _guarded((T, D), torch.bfloat16, 7.0)
+    bufs["mean"] = _guarded((T,), torch.float32, 7.0)
+    bufs["rstd"] = _guarded((T,), torch.float32, 7.0)
+    bufs["dshift"] = _guarded((nseg, D), torch.float32, 7.0)
+    bufs["dscale"] = _guarded((nseg, D), torch.float32, 7.0)
+    ws_bytes = adaln.adaln_bwd_workspace_size(T, D, nseg, torch.bfloat16)
+    bufs["ws"] = _guarded((ws_bytes,), torch.uint8, 0xA5)
+    adaln.adaln_fwd(d["x"], d["shift"], d["scale"], d["seg_id"], c["eps"],
+                    y=bufs["y"][1], mean=bufs["mean"][1], rstd=bufs["rstd"][1])
+    adaln.adaln_bwd(d["dy"], d["x"], bufs["mean"][1], bufs["rstd"][1], d["scale"], d["seg_id"],
+                    dx=bufs["dx"][1], dshift=bufs["dshift"][1], dscale=bufs["dscale"][1],
+                    workspace=bufs["ws"][1])
+    torch.cuda.synchronize()
+    for k, (buf, _, pad) in bufs.items():
+        fill = 0xA5 if k == "ws" else 7.0
+        assert torch.all(buf[:pad] == fill), k
+        assert torch.all(buf[-pad:] == fill), k
+    out = {k: bufs[k][1] for k in ("y", "dx", "mean", "rstd", "dshift", "dscale")}
+    H.check_against_oracle(c, d, out)
+
+
+def test_backward_is_bitwise_deterministic(adaln):
+    c = I.make(2)
+    d = H.device_inputs(c)
+    a = H.run_gpu(d, c["eps"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        junk = torch.randn(1 << 24, device="cuda")  # shift the stream position
+        b = H.run_gpu(d, c["eps"], stream=s)
+        del junk
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_bad_segment_ids_set_status_and_stay_in_bounds(adaln):
+    dev = "cuda"
+    T, D, nseg = 600, 256, 4
+    x = torch.randn(T, D, device=dev).to(torch.bfloat16)
+    sh = torch.randn(nseg, D, device=dev).to(torch.bfloat16)
+    for bad, bit in ((np.r_[np.zeros(300), np.ones(300) * 9], adaln.ADALN_DEV_SEG_RANGE),
+                     (np.r_[np.ones(300) * 2, np.zeros(300)], adaln.ADALN_DEV_SEG_ORDER),
+                     (np.r_[np.zeros(300), -np.ones(300)], adaln.ADALN_DEV_SEG_RANGE)):
+        seg = torch.from_numpy(bad.astype(np.int32)).to(dev)
+        y_buf, y, _ = _guarded((T, D), torch.bfloat16, 3.0)
+        y, m, r = adaln.adaln_fwd(x, sh, sh, seg, 1e-6, y=y)
+        rc, bits = adaln.adaln_get_status()
+        assert rc == adaln.ADALN_ERR_SEG and bits & bit, (rc, bits)
+        ws_bytes = adaln.adaln_bwd_workspace_size(T, D, nseg, torch.bfloat16)
+        ws_buf, ws, _ = _guarded((ws_bytes,), torch.uint8, 0x5A)
+        dsh_buf, dsh, _ = _guarded((nseg, D), torch.float32, 3.0)
+        adaln.adaln_bwd(x, x, m, r, sh, seg, dshift=dsh, workspace=ws)
+        rc, bits = adaln.adaln_get_status()
+        assert rc == adaln.ADALN_ERR_SEG and bits & bit, (rc, bits)
+        for buf, f in ((y_buf, 3.0), (ws_buf, 0x5A), (dsh_buf, 3.0)):
+            assert torch.all(buf[:4096] == f) and torch.all(buf[-4096:] == f)
+
+
+def test_workspace_and_alignment_errors(adaln):
+    dev = "cuda"
+    T, D, nseg = 64, 64, 1
+    x = torch.randn(T, D, device=dev).to(torch.bfloat16)
+    sh = torch.zeros(nseg, D, device=dev, dtype=torch.bfloat16)
+    seg = torch.zeros(T, device=dev, dtype=torch.int32)
+    y, m, r = adaln.adaln_fwd(x, sh, sh, seg, 1e-6)
+    need = adaln.adaln_bwd_workspace_size(T, D, nseg, torch.bfloat16)
+    small = torch.empty(need - 16, device=dev, dtype=torch.uint8)
+    with pytest.raises(adaln.AdalnError) as e:
+        adaln.adaln_bwd(x, x, m, r, sh, seg, workspace=small)
+    assert e.value.code == adaln.ADALN_ERR_WORKSPACE
+    flat = torch.empty(T * D + 8, device=dev, dtype=torch.bfloat16)
+    mis = flat[1:1 + T * D].view(T, D)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(adaln.AdalnError) as e:
+        adaln.adaln_fwd(mis, sh, sh, seg, 1e-6)
+    assert e.value.code == adaln.ADALN_ERR_ALIGN
+
+
+def test_trace_counts_launches(adaln):
+    c = I.random_case(5, 500, 512, 2, dtype="bf16")
+    d = H.device_inputs(c)
+    adaln.adaln_trace_begin(16)
+    for _ in range(3):
+        H.run_gpu(d, c["eps"])
+    adaln.adaln_trace_end()
+    for k in range(3):
+        n, ms = adaln.adaln_trace_get(k)
+        assert n == 3 and ms > 0.0, (k, n, ms)
+
+
+def test_launch_shape_matches_the_rules(adaln):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 32760, 5120, 1, torch.bfloat16)
+    assert s["threads"] == 11 * 32 and s["grid"] % sms == 0 and s["stages"] >= 2
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 5, 5120, 1, torch.bfloat16)
+    assert s["grid"] == 5
