@@ -74,6 +74,18 @@ def build(force=False, verbose=False, ptxas_info=False):
     return LIB
 
 
+
+def source_hash():
+    """sha256 over the CUDA sources and headers (identifies a kernel build)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(_deps()):
+        if f.endswith(".py"):
+            continue
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
                 ptxas_info="--ptxas" in sys.argv))
