@@ -22,7 +22,9 @@ ADALN_KERNEL_FWD, ADALN_KERNEL_BWD_ROWS, ADALN_KERNEL_BWD_FINALIZE = 0, 1, 2
 KERNEL_NAMES = {0: "adaln_fwd_kernel", 1: "adaln_bwd_rows_kernel",
                 2: "adaln_bwd_finalize_kernel"}
 
-EXPORTS = ["adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd",
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+EXPORTS = ["adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_noalloc",
            "adaln_get_status", "adaln_strerror", "adaln_trace_begin",
            "adaln_trace_end", "adaln_trace_get", "adaln_launch_shape"]
 
@@ -48,6 +50,8 @@ def _load():
     lib.adaln_bwd.restype = ci
     lib.adaln_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, ci, vp, vp, vp,
                               vp, ctypes.c_size_t, vp]
+    lib.adaln_bwd_noalloc.restype = ci
+    lib.adaln_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, ci, vp, vp, vp, vp]
     lib.adaln_get_status.restype = ci
     lib.adaln_get_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
     lib.adaln_strerror.restype = ctypes.c_char_p
@@ -164,6 +168,34 @@ def adaln_bwd(dy, x, mean, rstd, scale, seg_id, dx=None, dshift=None, dscale=Non
                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                        _stream_ptr(stream, x.device))
     _check(rc, "adaln_bwd")
+    return dx, dshift, dscale
+
+
+def adaln_bwd_noalloc(dy, x, mean, rstd, scale, seg_id, dx=None, dshift=None, dscale=None,
+                      stream=None):
+    """adaln_bwd without a workspace argument: for callers that cannot
+    allocate device memory, the library uses its fixed static scratch array
+    (ADALN_NOALLOC_SCRATCH_BYTES per device, shared by all calls; calls that
+    overlap on the GPU race).  Outputs are allocated here only when not
+    given; pass them in to allocate nothing."""
+    T, D = x.shape
+    nseg = scale.shape[0]
+    dt = x.dtype
+    _dev(dy, "dy", dt, (T, D))
+    _dev(x, "x", dt)
+    _dev(mean, "mean", torch.float32, (T,))
+    _dev(rstd, "rstd", torch.float32, (T,))
+    _dev(scale, "scale", dt, (nseg, D))
+    _dev(seg_id, "seg_id", torch.int32, (T,))
+    dx = torch.empty_like(x) if dx is None else _dev(dx, "dx", dt, (T, D))
+    dshift = (torch.empty(nseg, D, device=x.device, dtype=torch.float32) if dshift is None
+              else _dev(dshift, "dshift", torch.float32, (nseg, D)))
+    dscale = (torch.empty(nseg, D, device=x.device, dtype=torch.float32) if dscale is None
+              else _dev(dscale, "dscale", torch.float32, (nseg, D)))
+    rc = raw.adaln_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(scale),
+                               _ptr(seg_id), T, D, nseg, dtype_code(dt), _ptr(dx),
+                               _ptr(dshift), _ptr(dscale), _stream_ptr(stream, x.device))
+    _check(rc, "adaln_bwd_noalloc")
     return dx, dshift, dscale
 
 

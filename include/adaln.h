@@ -129,6 +129,29 @@ ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
               size_t workspace_bytes, void* stream);
 
 /*
+ * Backward that allocates nothing, for callers that cannot call cudaMalloc
+ * (for example code inside a host framework whose allocator owns all device
+ * memory, or code on a latency-critical path where allocating would
+ * synchronise the device).  The paper has no counterpart: this is a
+ * deployment variant of adaln_bwd.  Same arguments, results and launches as
+ * adaln_bwd, minus the workspace: the scratch is a fixed file-scope device
+ * array of ADALN_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the
+ * library until the process exits.  Sizes whose adaln_bwd_workspace_size
+ * exceeds it are rejected with ADALN_ERR_WORKSPACE before anything is
+ * launched.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the array and it
+ * keeps the last call's contents (nothing in it needs to start at zero);
+ * calls that overlap on the GPU race on it.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ */
+#define ADALN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+ADALN_API int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean,
+              const float* rstd, const void* scale, const int32_t* seg_id,
+              int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype,
+              void* dx, float* dshift, float* dscale, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word.
  * *host_bits (if non-NULL) receives the ADALN_DEV_* bits.  Returns ADALN_OK,
  * ADALN_ERR_SEG, ADALN_ERR_TIMEOUT or ADALN_ERR_CUDA.  The word is shared by
