@@ -148,7 +148,7 @@ int adaln_fwd(const void* x, const void* shift, const void* scale,
   unsigned* status = nullptr;
   e = status_ptr(&status);
   if (e != cudaSuccess) return cuda_fail(e);
-  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, status};
+  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, 1.0f / (float)D, status};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = traced(ADALN_KERNEL_FWD, st, [&] { return launch_fwd(a, dtype, s, st); });
   return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
@@ -162,7 +162,7 @@ int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t d
   Shape s;
   cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
-  const size_t need = (size_t)bwd_slots(s, nseg) * 2 * (size_t)D * sizeof(float);
+  const size_t need = bwd_workspace_bytes(s, D, nseg);
   *bytes = (need + 255) & ~(size_t)255;
   return ADALN_OK;
 }
@@ -185,14 +185,17 @@ int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rst
   Shape s;
   cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
-  const size_t need = (size_t)bwd_slots(s, nseg) * 2 * (size_t)D * sizeof(float);
+  const size_t need = bwd_workspace_bytes(s, D, nseg);
   if (workspace_bytes < need) return ADALN_ERR_WORKSPACE;
   unsigned* status = nullptr;
   e = status_ptr(&status);
   if (e != cudaSuccess) return cuda_fail(e);
 
+  float* partials = static_cast<float*>(workspace);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                                  bwd_partials_bytes(s, D, nseg));
   BwdArgs a{dy, x, mean, rstd, scale, seg_id, dx, dshift, dscale,
-            static_cast<float*>(workspace), T, D, nseg, status};
+            partials, seg_start, T, D, nseg, 1.0f / (float)D, status};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T > 0) {
     e = traced(ADALN_KERNEL_BWD_ROWS, st, [&] { return launch_bwd_rows(a, dtype, s, st); });

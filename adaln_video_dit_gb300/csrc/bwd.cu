@@ -23,50 +23,60 @@
 
 namespace adaln {
 
+// (1 + scale[b]) for this thread's columns, as fp32 pairs.
 template <class E, int VPT>
-__device__ __forceinline__ void load_one_plus_scale(const void* scale, int b, int j,
-                                                    int NT, int nvec,
-                                                    float (&s1)[VPT][E::EPV]) {
+__device__ __forceinline__ void load_one_plus_scale(const void* scale, int b, int j, int NT,
+                                                    const bool (&valid)[VPT], int nvec,
+                                                    float2 (&s1)[VPT][E::EPV / 2]) {
 #pragma unroll
   for (int q = 0; q < VPT; ++q) {
-    const int v = j + q * NT;
-    if (v < nvec) {
-      float f[E::EPV];
-      E::unpack(ld_global_v4(static_cast<const unsigned char*>(scale) +
-                             ((size_t)b * nvec + v) * 16), f);
+    if (valid[q]) {
+      E::unpack2(ld_global_v4(static_cast<const unsigned char*>(scale) +
+                              ((size_t)b * nvec + j + q * NT) * 16), s1[q]);
 #pragma unroll
-      for (int e = 0; e < E::EPV; ++e) s1[q][e] = 1.0f + f[e];
+      for (int e = 0; e < E::EPV / 2; ++e) s1[q][e] = add2(s1[q][e], splat2(1.0f));
     }
   }
 }
 
+// Write this thread's column sums as partial slot `slot`: [dscale | dshift].
 template <class E, int VPT>
-__device__ __forceinline__ void flush_partials(float* partials, int64_t slot, int D,
-                                               int j, int NT, int nvec,
-                                               float (&acc_s)[VPT][E::EPV],
-                                               float (&acc_b)[VPT][E::EPV]) {
+__device__ __forceinline__ void flush_partials(float* partials, int64_t slot, int D, int j,
+                                               int NT, const bool (&valid)[VPT],
+                                               const float2 (&acc_s)[VPT][E::EPV / 2],
+                                               const float2 (&acc_b)[VPT][E::EPV / 2]) {
   float* ps = partials + (size_t)slot * 2 * D;
   float* pb = ps + D;
 #pragma unroll
   for (int q = 0; q < VPT; ++q) {
-    const int v = j + q * NT;
-    if (v < nvec) {
+    if (valid[q]) {
+      const size_t c0 = (size_t)(j + q * NT) * E::EPV;
 #pragma unroll
-      for (int e = 0; e < E::EPV; e += 4) {
-        *reinterpret_cast<float4*>(ps + (size_t)v * E::EPV + e) =
-            make_float4(acc_s[q][e], acc_s[q][e + 1], acc_s[q][e + 2], acc_s[q][e + 3]);
-        *reinterpret_cast<float4*>(pb + (size_t)v * E::EPV + e) =
-            make_float4(acc_b[q][e], acc_b[q][e + 1], acc_b[q][e + 2], acc_b[q][e + 3]);
+      for (int e = 0; e < E::EPV / 2; e += 2) {
+        *reinterpret_cast<float4*>(ps + c0 + 2 * e) =
+            make_float4(acc_s[q][e].x, acc_s[q][e].y, acc_s[q][e + 1].x, acc_s[q][e + 1].y);
+        *reinterpret_cast<float4*>(pb + c0 + 2 * e) =
+            make_float4(acc_b[q][e].x, acc_b[q][e].y, acc_b[q][e + 1].x, acc_b[q][e + 1].y);
       }
     }
   }
 }
 
-template <class E, int VPT, int R>
-__global__ void __launch_bounds__(max_threads(VPT), 1)
+// Chunks of R rows per ring stage, R rows per reduction round.  Consumers
+// walk the CTA's rows as runs of equal segment id: an inner loop over the
+// chunks of one run (no flush inside, so the column accumulators stay in
+// registers) and the flush of the run's partial between runs.  A chunk that
+// a segment boundary splits is visited once per run, each visit handling its
+// rows of that run; its stage is released after the last visit.
+template <class E, int VARIANT, int R>
+__global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
     adaln_bwd_rows_kernel(BwdArgs a, int nc, int stages, int nvec) {
+  constexpr int VPT = variant_vpt(VARIANT);
+  constexpr int H = E::EPV / 2;
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int EPV = E::EPV;
+  // Let the finalize grid be scheduled as soon as SMs free up; it waits for
+  // this grid's completion before reading anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Ring rg = ring_layout(smem, stages);
   ring_init(rg, nc);
 
@@ -76,7 +86,7 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
   const int row_bytes = nvec * 16;
   const int warp = threadIdx.x >> 5;
 
-  if (warp == nc) {  // producer warp: x and dy rows into each stage
+  if (warp == nc) {  // producer warp: R rows of x, then R rows of dy, per stage
     if ((threadIdx.x & 31) == 0) {
       const unsigned char* src[2] = {
           static_cast<const unsigned char*>(a.x) + (size_t)r0 * row_bytes,
@@ -91,180 +101,247 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
   const int64_t nchunks = (nrows + R - 1) / R;
   const uint32_t ring0 = smem_addr(rg.ring);
   const uint32_t stage_bytes = (uint32_t)R * row_bytes * 2;
+  bool valid[VPT];
+#pragma unroll
+  for (int q = 0; q < VPT; ++q) valid[q] = j + q * NT < nvec;
 
-  float acc_s[VPT][EPV], acc_b[VPT][EPV], s1[VPT][EPV];
-#pragma unroll
-  for (int q = 0; q < VPT; ++q)
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) acc_s[q][e] = acc_b[q][e] = s1[q][e] = 0.0f;
-  int acc_seg = -1;  // segment whose sums are in acc_s / acc_b
-  int s1_seg = -1;   // segment whose (1 + scale) is in s1
-  int prev_b = 0;
+  float2 acc_s[VPT][H], acc_b[VPT][H], s1[VPT][H];
+  int s1_seg = -1;  // segment whose (1 + scale) is in s1
+  // Clamped segment of the row before the current chunk (-1 before row 0).
+  int prev_last = -1;
   if (r0 > 0) {
     int p = a.seg[r0 - 1];
-    prev_b = p < 0 ? 0 : (p >= a.nseg ? a.nseg - 1 : p);
+    prev_last = p < 0 ? 0 : (p >= a.nseg ? a.nseg - 1 : p);
   }
   int phase = 0;
   bool aborted = false;
 
-  for (int64_t k = 0; k < nchunks; ++k) {
-    const int s = (int)(k % stages);
-    const uint32_t par = (uint32_t)((k / stages) & 1);
-    const int rows = (int)min((int64_t)R, nrows - k * R);
-    const int64_t t0 = r0 + k * R;
-    int sg[R];
-    float mu[R], rs[R];
+  // Row metadata of the current chunk (cb: clamped segment ids) and, loaded
+  // one chunk ahead so the latency hides behind a chunk's work, of the next.
+  int cb[R], nb[R];
+  float cmu[R], crs[R], nmu[R], nrs[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const bool in = r < rows;
-      sg[r] = in ? __ldg(a.seg + t0 + r) : 0;
-      mu[r] = in ? __ldg(a.mean + t0 + r) : 0.0f;
-      rs[r] = in ? __ldg(a.rstd + t0 + r) : 0.0f;
-    }
-
-    // The stage stays in use until phase 2 has read it: x and dy are read
-    // from shared memory in both phases instead of being held in registers.
-    const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
-    const uint32_t st0 = ring0 + s * stage_bytes;
-
-    // Phase 1 (rows in order): segment bookkeeping, column sums, row partials.
-    float part[R][2];
-    int bs[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      part[r][0] = part[r][1] = 0.0f;
-      bs[r] = 0;
-      if (r < rows && ok) {
-        const int b = checked_seg(sg[r], prev_b, a.nseg, a.status);
-        prev_b = b;
-        bs[r] = b;
-        if (b != acc_seg) {
-          if (acc_seg >= 0)
-            flush_partials<E, VPT>(a.partials, blockIdx.x + acc_seg, a.D, j, NT, nvec, acc_s, acc_b);
-#pragma unroll
-          for (int q = 0; q < VPT; ++q)
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) acc_s[q][e] = acc_b[q][e] = 0.0f;
-          acc_seg = b;
-        }
-        if (b != s1_seg) {
-          load_one_plus_scale<E, VPT>(a.scale, b, j, NT, nvec, s1);
-          s1_seg = b;
-        }
-#pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          if (j + q * NT < nvec) {
-            const int v = j + q * NT;
-            float fx[EPV], fd[EPV];
-            E::unpack(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), fx);
-            E::unpack(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const float xh = (fx[e] - mu[r]) * rs[r];
-              const float g = fd[e] * s1[q][e];
-              part[r][0] += g;
-              part[r][1] = fmaf(g, xh, part[r][1]);
-              acc_s[q][e] = fmaf(fd[e], xh, acc_s[q][e]);
-              acc_b[q][e] += fd[e];
-            }
-          }
-        }
-      }
-    }
-    if (!team_sum<R, 2>(part, ok, rg, nc, phase)) {
-      if (j == 0) {
-        atomicOr(a.status, ADALN_DEV_TIMEOUT);
-        *rg.abort = 1;
-      }
-      aborted = true;
-      break;
-    }
-    phase ^= 1;
-
-    // Phase 2 (rows in reverse, so a mid-chunk segment change reloads the
-    // scale vector at most once more): dx.
-#pragma unroll
-    for (int r = R - 1; r >= 0; --r) {
-      if (r < rows) {
-        const int64_t t = t0 + r;
-        if (bs[r] != s1_seg) {
-          load_one_plus_scale<E, VPT>(a.scale, bs[r], j, NT, nvec, s1);
-          s1_seg = bs[r];
-        }
-        const float mg = part[r][0] / (float)a.D;
-        const float mgx = part[r][1] / (float)a.D;
-#pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          const int v = j + q * NT;
-          if (v < nvec) {
-            float fx[EPV], fd[EPV];
-            E::unpack(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), fx);
-            E::unpack(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              const float xh = (fx[e] - mu[r]) * rs[r];
-              const float g = fd[e] * s1[q][e];
-              fx[e] = rs[r] * (g - mg - xh * mgx);
-            }
-            st_global_cs_v4(static_cast<unsigned char*>(a.dx) + ((size_t)t * nvec + v) * 16,
-                            E::pack(fx));
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
+  for (int r = 0; r < R; ++r) {
+    const bool in = r < nrows;
+    nb[r] = in ? __ldg(a.seg + r0 + r) : 0;
+    nmu[r] = in ? __ldg(a.mean + r0 + r) : 0.0f;
+    nrs[r] = in ? __ldg(a.rstd + r0 + r) : 0.0f;
   }
-  if (!aborted && acc_seg >= 0)
-    flush_partials<E, VPT>(a.partials, blockIdx.x + acc_seg, a.D, j, NT, nvec, acc_s, acc_b);
+  // Move the prefetched metadata of chunk kk into cb/cmu/crs (checking the
+  // segment ids), then start loading chunk kk + 1.
+  auto advance = [&](int64_t kk) {
+    const int rows = (int)min((int64_t)R, nrows - kk * R);
+    int before = prev_last < 0 ? 0 : prev_last;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      cmu[r] = nmu[r];
+      crs[r] = nrs[r];
+      cb[r] = 0;
+      if (r < rows) {
+        cb[r] = checked_seg(nb[r], before, a.nseg, a.status);
+        before = cb[r];
+      }
+      const int64_t u = (kk + 1) * R + r;
+      const bool in = u < nrows;
+      nb[r] = in ? __ldg(a.seg + r0 + u) : 0;
+      nmu[r] = in ? __ldg(a.mean + r0 + u) : 0.0f;
+      nrs[r] = in ? __ldg(a.rstd + r0 + u) : 0.0f;
+    }
+  };
+  advance(0);
+
+  int64_t k = 0;  // current chunk
+  int lo = 0;     // first row of chunk k not yet processed
+  bool ok = true;
+  while (k < nchunks && !aborted) {
+    // Start a run at row (k, lo).  Its first row is recorded in the segment
+    // start table, together with that of every empty segment between the
+    // previous row's segment and this one (each entry has one writer: the CTA
+    // owning the row).
+    int run_seg = cb[0];
+    int before = prev_last;
+#pragma unroll
+    for (int r = 1; r < R; ++r)
+      if (r == lo) { run_seg = cb[r]; before = cb[r - 1]; }
+    for (int b = before + 1 + j; b <= run_seg; b += NT)
+      a.seg_start[b] = (int32_t)(r0 + k * R + lo);
+#pragma unroll
+    for (int q = 0; q < VPT; ++q)
+#pragma unroll
+      for (int e = 0; e < H; ++e) acc_s[q][e] = acc_b[q][e] = make_float2(0.f, 0.f);
+    if (run_seg != s1_seg) {
+      load_one_plus_scale<E, VPT>(a.scale, run_seg, j, NT, valid, nvec, s1);
+      s1_seg = run_seg;
+    }
+
+    while (k < nchunks) {
+      const int rows = (int)min((int64_t)R, nrows - k * R);
+      // Rows [lo, hi) of this chunk belong to the run.
+      int hi = lo;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r == hi && r < rows && cb[r] == run_seg) hi = r + 1;
+      if (hi == lo) break;  // row lo starts the next run
+
+      const int s = (int)(k % stages);
+      if (lo == 0) ok = mbar_wait_bounded(rg.full(s), (uint32_t)((k / stages) & 1), rg.abort);
+      const uint32_t st0 = ring0 + s * stage_bytes;
+
+      // Phase 1: xhat, g; column sums; the two row partials.
+      float part[R][2];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        part[r][0] = part[r][1] = 0.0f;
+        if (ok && r >= lo && r < hi) {
+          const float2 nm = splat2(-cmu[r]), r2 = splat2(crs[r]);
+          float2 p0 = make_float2(0.f, 0.f), p1 = p0;
+#pragma unroll
+          for (int q = 0; q < VPT; ++q) {
+            if (valid[q]) {
+              const int v = j + q * NT;
+              float2 fx[H], fd[H];
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), fx);
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
+#pragma unroll
+              for (int e = 0; e < H; ++e) {
+                const float2 xh = mul2(add2(fx[e], nm), r2);
+                const float2 g = mul2(fd[e], s1[q][e]);
+                p0 = add2(p0, g);
+                p1 = fma2(g, xh, p1);
+                acc_s[q][e] = fma2(fd[e], xh, acc_s[q][e]);
+                acc_b[q][e] = add2(acc_b[q][e], fd[e]);
+              }
+            }
+          }
+          part[r][0] = p0.x + p0.y;
+          part[r][1] = p1.x + p1.y;
+        }
+      }
+      if (!team_sum<R, 2>(part, ok, rg, nc, phase)) {
+        if (j == 0) {
+          atomicOr(a.status, ADALN_DEV_TIMEOUT);
+          *rg.abort = 1;
+        }
+        aborted = true;
+        break;
+      }
+      phase ^= 1;
+
+      // Phase 2: dx = rstd (g - mean g - xhat mean(g xhat)).
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (r >= lo && r < hi) {
+          const int64_t t = r0 + k * R + r;
+          const float2 nm = splat2(-cmu[r]), r2 = splat2(crs[r]);
+          const float2 nmg = splat2(-part[r][0] * a.inv_d);
+          const float2 nmgx = splat2(-part[r][1] * a.inv_d);
+#pragma unroll
+          for (int q = 0; q < VPT; ++q) {
+            if (valid[q]) {
+              const int v = j + q * NT;
+              float2 fx[H], fd[H];
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), fx);
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
+#pragma unroll
+              for (int e = 0; e < H; ++e) {
+                const float2 xh = mul2(add2(fx[e], nm), r2);
+                const float2 g = mul2(fd[e], s1[q][e]);
+                fx[e] = mul2(fma2(xh, nmgx, add2(g, nmg)), r2);
+              }
+              st_global_cs_v4(static_cast<unsigned char*>(a.dx) + ((size_t)t * nvec + v) * 16,
+                              E::pack2(fx));
+            }
+          }
+        }
+      }
+
+      if (hi < rows) {  // a segment boundary inside the chunk: next run
+        lo = hi;
+        break;
+      }
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r == rows - 1) prev_last = cb[r];
+      ++k;
+      lo = 0;
+      if (k < nchunks) advance(k);
+    }
+    if (!aborted)
+      flush_partials<E, VPT>(a.partials, blockIdx.x + run_seg, a.D, j, NT, valid, acc_s, acc_b);
+  }
+  // The CTA owning the last row closes the table: segments after the last
+  // one present start (and end) at T.
+  if (!aborted && r0 + nrows == a.T)
+    for (int b = prev_last + 1 + j; b <= a.nseg; b += NT) a.seg_start[b] = (int32_t)a.T;
 }
 
-// Sum the partials of each segment in CTA order.  Block (b, column block):
-// 32 float4 columns x J warps; warp w sums a contiguous run of the segment's
-// CTAs, then warp 0 adds the J results in warp order.
-__global__ void __launch_bounds__(32 * 16)
+// Sum the partials of each segment in CTA order.  Block (b, column block of
+// 8 float4 columns) has J warps; lane l handles column (l & 7) of the block
+// and slot group g = 4 w + (l >> 3) of 4J groups, each a contiguous run of
+// the segment's CTAs summed in order; thread group g = 0 then adds the 4J
+// group sums in group order.  The order of every sum is fixed by (T, G,
+// nseg), so results are bitwise reproducible.  Launched as a programmatic
+// dependent of the row pass: it waits (griddepcontrol.wait) until the row
+// pass has completed and its writes are visible.
+constexpr int kFinalizeMaxWarps = 8;
+
+__global__ void __launch_bounds__(32 * kFinalizeMaxWarps)
     adaln_bwd_finalize_kernel(BwdArgs a, int G, int J) {
-  __shared__ float4 sh_s[16][32], sh_b[16][32];
+  __shared__ float4 sh_s[4 * kFinalizeMaxWarps][8], sh_b[4 * kFinalizeMaxWarps][8];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int ncol4 = a.D / 4;
-  const int col4 = blockIdx.y * 32 + lane;
+  const int col4 = blockIdx.y * 8 + (lane & 7);
+  const int g = 4 * w + (lane >> 3), ng = 4 * J;
 
-  // Rows of segment b: [lower_bound(b), lower_bound(b + 1)).
+  // Rows of segment b: [seg_start[b], seg_start[b + 1]), recorded by the
+  // row pass.  Clamped so that inconsistent input (reported in the status
+  // word) still reads inside the workspace.
   int64_t sb = 0, eb = 0;
-  {
-    int64_t lo = 0, hi = a.T;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (__ldg(a.seg + mid) < b) lo = mid + 1; else hi = mid;
-    }
-    sb = lo;
-    hi = a.T;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (__ldg(a.seg + mid) < b + 1) lo = mid + 1; else hi = mid;
-    }
-    eb = lo;
+  if (a.T > 0) {
+    sb = a.seg_start[b];
+    eb = a.seg_start[b + 1];
+    sb = sb < 0 ? 0 : (sb > a.T ? a.T : sb);
+    eb = eb < 0 ? 0 : (eb > a.T ? a.T : eb);
   }
   float4 ps = make_float4(0.f, 0.f, 0.f, 0.f), pb = ps;
   if (eb > sb && col4 < ncol4) {
     const int64_t c0 = part_owner(sb, a.T, G), c1 = part_owner(eb - 1, a.T, G);
     const int64_t n = c1 - c0 + 1;
-    const int64_t lo = c0 + (n * w) / J, hi = c0 + (n * (w + 1)) / J;
-    const size_t D2 = 2 * (size_t)a.D;
-    for (int64_t c = lo; c < hi; ++c) {
-      const float4* p = reinterpret_cast<const float4*>(a.partials + (size_t)(c + b) * D2);
-      const float4 u = p[col4], v = p[ncol4 + col4];
+    const int64_t lo = c0 + (n * g) / ng, hi = c0 + (n * (g + 1)) / ng;
+    const size_t row4 = 2 * (size_t)a.D / 4;  // float4 per slot
+    const float4* base = reinterpret_cast<const float4*>(a.partials) + col4;
+    int64_t c = lo;
+    for (; c + 4 <= hi; c += 4) {
+      float4 u[4], v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4* p = base + (size_t)(c + i + b) * row4;
+        u[i] = __ldcs(p);
+        v[i] = __ldcs(p + ncol4);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ps.x += u[i].x; ps.y += u[i].y; ps.z += u[i].z; ps.w += u[i].w;
+        pb.x += v[i].x; pb.y += v[i].y; pb.z += v[i].z; pb.w += v[i].w;
+      }
+    }
+    for (; c < hi; ++c) {
+      const float4* p = base + (size_t)(c + b) * row4;
+      const float4 u = __ldcs(p), v = __ldcs(p + ncol4);
       ps.x += u.x; ps.y += u.y; ps.z += u.z; ps.w += u.w;
       pb.x += v.x; pb.y += v.y; pb.z += v.z; pb.w += v.w;
     }
   }
-  sh_s[w][lane] = ps;
-  sh_b[w][lane] = pb;
+  sh_s[g][lane & 7] = ps;
+  sh_b[g][lane & 7] = pb;
   __syncthreads();
-  if (w == 0 && col4 < ncol4) {
+  if (threadIdx.x < 8 && col4 < ncol4) {
     float4 ts = sh_s[0][lane], tb = sh_b[0][lane];
-    for (int i = 1; i < J; ++i) {
+    for (int i = 1; i < ng; ++i) {
       const float4 u = sh_s[i][lane], v = sh_b[i][lane];
       ts.x += u.x; ts.y += u.y; ts.z += u.z; ts.w += u.w;
       tb.x += v.x; tb.y += v.y; tb.z += v.z; tb.w += v.w;
@@ -282,37 +359,31 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 
 namespace {
 
-// Rows per reduction round of the backward: 2, except 1 for the widest rows
-// (VPT = 4), whose column accumulators already fill the register budget.
-constexpr int bwd_rows_per_round(int vpt) { return vpt == 4 ? 1 : kRowsPerRound; }
-
-template <class E, int VPT>
-void* rows_kernel_ptr() {
-  return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, VPT, bwd_rows_per_round(VPT)>);
-}
-
 template <class E>
-void* pick_rows_e(int vpt) {
-  return vpt == 1 ? rows_kernel_ptr<E, 1>()
-                  : (vpt == 2 ? rows_kernel_ptr<E, 2>() : rows_kernel_ptr<E, 4>());
+void* rows_kernel_for(int variant) {
+  switch (variant) {
+    case 0: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 0, kBwdRows>);
+    case 1: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 1, kBwdRows>);
+    case 2: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 2, kBwdRows>);
+    default: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 3, kBwdRows>);
+  }
 }
 
-void* pick_rows(adaln_dtype_t dt, int vpt) {
-  return dt == ADALN_BF16 ? pick_rows_e<BF16>(vpt) : pick_rows_e<F32>(vpt);
+void* pick_rows(adaln_dtype_t dt, int variant) {
+  return dt == ADALN_BF16 ? rows_kernel_for<BF16>(variant) : rows_kernel_for<F32>(variant);
 }
 
 }  // namespace
 
 cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
-  const int nvec = D * esize / 16;
-  const int vpt = choose_vpt(nvec);
-  return staging_shape(pick_rows(dt, vpt), T, D, dt, 2, bwd_rows_per_round(vpt), s);
+  const int variant = choose_variant(D * esize / 16);
+  return staging_shape(pick_rows(dt, variant), T, D, dt, 2, kBwdRows, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
                             cudaStream_t st) {
-  void* k = pick_rows(dt, s.vpt);
+  void* k = pick_rows(dt, s.variant);
   int nc = s.nc, stages = s.stages, nvec = s.nvec;
   BwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec};
@@ -320,17 +391,28 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
 }
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {
-  // Warps per block: about 8 partials per warp for a segment spanning all
-  // CTAs, fewer when many segments share the CTAs.
+  // Warps per block: about 8 partials per slot group for a segment spanning
+  // all CTAs, a single warp when many segments share the CTAs.
   const int64_t per_seg = ((int64_t)s.grid + a.nseg - 1) / a.nseg;
-  int J = (int)((per_seg + 7) / 8);
-  J = J < 1 ? 1 : (J > 16 ? 16 : J);
+  int J = (int)((per_seg + 31) / 32);
+  J = J < 1 ? 1 : (J > kFinalizeMaxWarps ? kFinalizeMaxWarps : J);
   int G = s.grid;
   BwdArgs args = a;
   void* params[] = {&args, &G, &J};
-  const dim3 grid((unsigned)a.nseg, (unsigned)((a.D / 4 + 31) / 32));
-  return cudaLaunchKernel(reinterpret_cast<void*>(&adaln_bwd_finalize_kernel), grid,
-                          dim3(32 * J), params, 0, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((a.D / 4 + 7) / 8));
+  cfg.blockDim = dim3(32 * J);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  // Programmatic dependent launch: the launch overlaps the row pass's tail;
+  // the kernel itself waits for the row pass's results.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&adaln_bwd_finalize_kernel),
+                             params);
 }
 
 }  // namespace adaln

@@ -18,20 +18,19 @@ struct BF16 {
   static constexpr int EPV = 8;  // elements per 16-byte vector
   static constexpr int SIZE = 2;
   // Exact widening: a bf16 value is the upper half of an fp32 bit pattern.
-  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+  // Element 2i is the low half of word i.
+  __device__ static __forceinline__ void unpack2(const uint4& v, float2 (&f)[4]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; ++i)
+      f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
   }
   // Round to nearest even, once.
-  __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+  __device__ static __forceinline__ uint4 pack2(const float2 (&f)[4]) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      __nv_bfloat162 h = __floats2bfloat162_rn(f[i].x, f[i].y);
       w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -41,17 +40,21 @@ struct BF16 {
 struct F32 {
   static constexpr int EPV = 4;
   static constexpr int SIZE = 4;
-  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
+  __device__ static __forceinline__ void unpack2(const uint4& v, float2 (&f)[2]) {
+    f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
   }
-  __device__ static __forceinline__ uint4 pack(const float (&f)[4]) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  __device__ static __forceinline__ uint4 pack2(const float2 (&f)[2]) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                      __float_as_uint(f[1].x), __float_as_uint(f[1].y));
   }
 };
+
+// Packed fp32x2 arithmetic (one instruction per pair on sm_100 and later).
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // ---------------------------------------------------------------------------
 // Plain memory helpers.

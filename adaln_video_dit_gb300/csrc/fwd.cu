@@ -5,19 +5,23 @@
 // modulation is applied in the same launch, so x is read from HBM once and y
 // written once.  Here each persistent CTA streams its contiguous row range
 // through a shared-memory ring (bulk async copies issued by one producer
-// lane); consumer threads hold their column slice of R rows in registers,
-// compute the row mean, then the centred sum of squares (two-pass, exact
-// definition of the biased variance), and write y with 16-byte streaming
-// stores.
+// lane); consumer threads move their column slice of R rows into registers
+// once (widened to fp32), compute the row mean, then the centred sum of
+// squares (two-pass: the exact definition of the biased variance), and write
+// y with 16-byte streaming stores.  Element arithmetic uses packed fp32x2
+// instructions.
+#include <cstdlib>
+
 #include "ring.cuh"
 
 namespace adaln {
 
-template <class E, int VPT, int R>
-__global__ void __launch_bounds__(max_threads(VPT), 1)
+template <class E, int VARIANT, int R>
+__global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
     adaln_fwd_kernel(FwdArgs a, int nc, int stages, int nvec) {
+  constexpr int VPT = variant_vpt(VARIANT);
+  constexpr int H = E::EPV / 2;  // float2 pairs per vector
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int EPV = E::EPV;
   const Ring rg = ring_layout(smem, stages);
   ring_init(rg, nc);
 
@@ -41,9 +45,12 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
   const int64_t nchunks = (nrows + R - 1) / R;
   const uint32_t ring0 = smem_addr(rg.ring);
   const uint32_t stage_bytes = (uint32_t)R * row_bytes;
+  bool valid[VPT];
+#pragma unroll
+  for (int q = 0; q < VPT; ++q) valid[q] = j + q * NT < nvec;
 
-  // Modulation of the current segment for this thread's columns.
-  float s1[VPT][EPV], sh[VPT][EPV];
+  // (1 + scale) and shift of the current segment for this thread's columns.
+  float2 s1[VPT][H], sh[VPT][H];
   int cur_b = -1;
   int prev_b = 0;
   if (r0 > 0) {
@@ -52,6 +59,12 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
   }
   int phase = 0;
 
+  // Segment ids are loaded one chunk ahead, so their latency hides behind
+  // the current chunk's work.
+  int n_sg[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) n_sg[r] = r < nrows ? __ldg(a.seg + r0 + r) : 0;
+
   for (int64_t k = 0; k < nchunks; ++k) {
     const int s = (int)(k % stages);
     const uint32_t par = (uint32_t)((k / stages) & 1);
@@ -59,35 +72,35 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
     const int64_t t0 = r0 + k * R;
     int sg[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) sg[r] = r < rows ? __ldg(a.seg + t0 + r) : 0;
+    for (int r = 0; r < R; ++r) {
+      sg[r] = n_sg[r];
+      const int64_t u = (k + 1) * R + r;
+      n_sg[r] = u < nrows ? __ldg(a.seg + r0 + u) : 0;
+    }
 
+    // x stays in the stage until the outputs are written: each pass reads
+    // its rows from shared memory (registers hold only column state).
     const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
-    uint4 xv[R][VPT];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int q = 0; q < VPT; ++q) {
-        const int v = j + q * NT;
-        xv[r][q] = make_uint4(0, 0, 0, 0);
-        if (ok && r < rows && v < nvec)
-          xv[r][q] = ld_shared_v4(ring0 + s * stage_bytes + (uint32_t)(r * nvec + v) * 16);
-      }
-    __syncwarp();
-    if (ok && (threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
+    const uint32_t st0 = ring0 + s * stage_bytes;
 
     // Pass 1: row sums -> mean.
     float acc[R][1];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float t = 0.0f;
+      float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (ok && r < rows) {
 #pragma unroll
-      for (int q = 0; q < VPT; ++q) {
-        float f[EPV];
-        E::unpack(xv[r][q], f);
+        for (int q = 0; q < VPT; ++q) {
+          if (valid[q]) {
+            float2 f[H];
+            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) t += f[e];
+            for (int e = 0; e < H; ++e) t[e & 1] = add2(t[e & 1], f[e]);
+          }
+        }
       }
-      acc[r][0] = t;
+      t[0] = add2(t[0], t[1]);
+      acc[r][0] = t[0].x + t[0].y;
     }
     if (!team_sum<R, 1>(acc, ok, rg, nc, phase)) {
       if (j == 0) {
@@ -99,25 +112,29 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
     phase ^= 1;
     float mu[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) mu[r] = acc[r][0] / (float)a.D;
+    for (int r = 0; r < R; ++r) mu[r] = acc[r][0] * a.inv_d;
 
     // Pass 2: centred sum of squares -> rstd.
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float t = 0.0f;
+      const float2 nm = splat2(-mu[r]);
+      float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (r < rows) {
 #pragma unroll
-      for (int q = 0; q < VPT; ++q) {
-        if (j + q * NT < nvec) {
-          float f[EPV];
-          E::unpack(xv[r][q], f);
+        for (int q = 0; q < VPT; ++q) {
+          if (valid[q]) {
+            float2 f[H];
+            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float c = f[e] - mu[r];
-            t = fmaf(c, c, t);
+            for (int e = 0; e < H; ++e) {
+              const float2 c = add2(f[e], nm);
+              t[e & 1] = fma2(c, c, t[e & 1]);
+            }
           }
         }
       }
-      acc[r][0] = t;
+      t[0] = add2(t[0], t[1]);
+      acc[r][0] = t[0].x + t[0].y;
     }
     team_sum<R, 1>(acc, true, rg, nc, phase);
     phase ^= 1;
@@ -125,46 +142,45 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
     // Modulate and store.
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      if (r >= rows) break;
-      const int64_t t = t0 + r;
-      const float rs = 1.0f / sqrtf(acc[r][0] / (float)a.D + a.eps);
-      const int b = checked_seg(sg[r], prev_b, a.nseg, a.status);
-      prev_b = b;
-      if (b != cur_b) {
-        cur_b = b;
+      if (r < rows) {
+        const int64_t t = t0 + r;
+        const float rs = rsqrtf(fmaf(acc[r][0], a.inv_d, a.eps));
+        const int b = checked_seg(sg[r], prev_b, a.nseg, a.status);
+        prev_b = b;
+        if (b != cur_b) {
+          cur_b = b;
 #pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          const int v = j + q * NT;
-          if (v < nvec) {
-            const size_t off = ((size_t)b * nvec + v) * 16;
-            float fs[EPV], fh[EPV];
-            E::unpack(ld_global_v4(static_cast<const unsigned char*>(a.scale) + off), fs);
-            E::unpack(ld_global_v4(static_cast<const unsigned char*>(a.shift) + off), fh);
+          for (int q = 0; q < VPT; ++q) {
+            if (valid[q]) {
+              const size_t off = ((size_t)b * nvec + j + q * NT) * 16;
+              E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.scale) + off), s1[q]);
+              E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.shift) + off), sh[q]);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-              s1[q][e] = 1.0f + fs[e];
-              sh[q][e] = fh[e];
+              for (int e = 0; e < H; ++e) s1[q][e] = add2(s1[q][e], splat2(1.0f));
             }
           }
         }
-      }
+        const float2 nm = splat2(-mu[r]), rs2 = splat2(rs);
 #pragma unroll
-      for (int q = 0; q < VPT; ++q) {
-        const int v = j + q * NT;
-        if (v < nvec) {
-          float f[EPV];
-          E::unpack(xv[r][q], f);
+        for (int q = 0; q < VPT; ++q) {
+          if (valid[q]) {
+            const int v = j + q * NT;
+            float2 f[H];
+            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), f);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) f[e] = fmaf((f[e] - mu[r]) * rs, s1[q][e], sh[q][e]);
-          st_global_cs_v4(static_cast<unsigned char*>(a.y) + ((size_t)t * nvec + v) * 16,
-                          E::pack(f));
+            for (int e = 0; e < H; ++e) f[e] = fma2(mul2(add2(f[e], nm), rs2), s1[q][e], sh[q][e]);
+            st_global_cs_v4(static_cast<unsigned char*>(a.y) + ((size_t)t * nvec + v) * 16,
+                            E::pack2(f));
+          }
+        }
+        if (j == 0) {
+          a.mean[t] = mu[r];
+          a.rstd[t] = rs;
         }
       }
-      if (j == 0) {
-        a.mean[t] = mu[r];
-        a.rstd[t] = rs;
-      }
     }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
   }
 }
 
@@ -173,49 +189,61 @@ __global__ void __launch_bounds__(max_threads(VPT), 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-template <class E, int VPT>
-void* fwd_kernel_ptr() {
-  return reinterpret_cast<void*>(&adaln_fwd_kernel<E, VPT, kRowsPerRound>);
-}
-
 template <class E>
-void* pick_fwd_e(int vpt) {
-  return vpt == 1 ? fwd_kernel_ptr<E, 1>()
-                  : (vpt == 2 ? fwd_kernel_ptr<E, 2>() : fwd_kernel_ptr<E, 4>());
+void* fwd_kernel_for(int variant) {
+  switch (variant) {
+    case 0: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 0, kFwdRows>);
+    case 1: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 1, kFwdRows>);
+    case 2: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 2, kFwdRows>);
+    default: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 3, kFwdRows>);
+  }
 }
 
-void* pick_fwd(adaln_dtype_t dt, int vpt) {
-  return dt == ADALN_BF16 ? pick_fwd_e<BF16>(vpt) : pick_fwd_e<F32>(vpt);
+void* pick_fwd(adaln_dtype_t dt, int variant) {
+  return dt == ADALN_BF16 ? fwd_kernel_for<BF16>(variant) : fwd_kernel_for<F32>(variant);
 }
 
 }  // namespace
 
-// Common shape rule of the staging kernels: vectors per thread (1, 2 or 4),
-// consumer warps, ring depth sized for roughly `ring_target` bytes in flight
-// per SM, and persistent CTAs = SMs x resident CTAs per SM (at most T).
+// Common shape rule of the staging kernels: the compiled variant for the row
+// length, consumer warps to cover the row, ring depth sized for about 160 KB
+// of staged rows per SM, and persistent CTAs = SMs x resident CTAs per SM
+// (at most T).
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
                           int ntensors, int rows_per_round, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   s->row_bytes = D * esize;
   s->nvec = s->row_bytes / 16;
-  s->vpt = choose_vpt(s->nvec);
+  s->variant = choose_variant(s->nvec);
+  s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
   s->threads = (s->nc + 1) * 32;
 
-  int dev = 0, sms = 0, optin = 0;
+  int dev = 0, sms = 0, optin = 0, smem_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
 
-  // Target CTAs per SM by warps (about 16 resident warps), then ring depth.
-  const int ctas_target = s->nc + 1 >= 16 ? 1 : 16 / (s->nc + 1);
-  const int ring_target = 160 * 1024 / ctas_target;
+  // Ring depth: about 160 KB of staged rows per SM (ADALN_RING_KB overrides,
+  // for launch-shape sweeps), split over the CTAs the variant is sized for,
+  // and no more than fits beside them.
+  const int ctas = variant_min_blocks(s->variant);
   const int stage_bytes = rows_per_round * s->row_bytes * ntensors;
-  int stages = ring_target / stage_bytes;
+  const int per_cta = smem_sm / ctas - 2048;  // room for the per-CTA reserve
+  int ring_kb = 160;
+  if (const char* env = getenv("ADALN_RING_KB")) {
+    const int v = atoi(env);
+    if (v >= 16 && v <= 256) ring_kb = v;
+  }
+  int budget = ring_kb * 1024 / ctas;
+  if (budget > per_cta) budget = per_cta;
+  int stages = budget / stage_bytes;
   stages = stages < 2 ? 2 : (stages > 16 ? 16 : stages);
-  while (stages > 2 && ring_header_bytes(stages) + stages * stage_bytes > optin) --stages;
+  while (stages > 2 && ring_header_bytes(stages) + stages * stage_bytes > per_cta) --stages;
   s->stages = stages;
   s->smem = ring_header_bytes(stages) + stages * stage_bytes;
   if (s->smem > optin) return cudaErrorInvalidValue;
@@ -228,6 +256,11 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, s->threads, s->smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // ADALN_CTAS_PER_SM lowers the resident CTAs per SM (launch-shape sweeps).
+  if (const char* env = getenv("ADALN_CTAS_PER_SM")) {
+    const int v = atoi(env);
+    if (v >= 1 && v < per_sm) per_sm = v;
+  }
   int64_t g = (int64_t)sms * per_sm;
   if (g > T) g = T;
   s->grid = (int)(g < 1 ? 1 : g);
@@ -236,13 +269,13 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 
 cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
-  const int nvec = D * esize / 16;
-  return staging_shape(pick_fwd(dt, choose_vpt(nvec)), T, D, dt, 1, kRowsPerRound, s);
+  const int variant = choose_variant(D * esize / 16);
+  return staging_shape(pick_fwd(dt, variant), T, D, dt, 1, kFwdRows, s);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st) {
-  void* k = pick_fwd(dt, s.vpt);
+  void* k = pick_fwd(dt, s.variant);
   int nc = s.nc, stages = s.stages, nvec = s.nvec;
   FwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec};

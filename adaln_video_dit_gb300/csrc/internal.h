@@ -15,27 +15,35 @@
 
 namespace adaln {
 
-// Rows handled per reduction round (compile-time in the kernels).
-constexpr int kRowsPerRound = 2;
-// Largest number of consumer warps in a CTA (any VPT).
-constexpr int kMaxConsumerWarps = 16;
+// Most rows handled per reduction round (compile-time in the kernels):
+// the forward takes 4 rows per round, the backward 2.
+constexpr int kRowsPerRound = 4;
+constexpr int kFwdRows = 4;
+constexpr int kBwdRows = 2;
+// Largest number of consumer warps in a CTA (any variant).
+constexpr int kMaxConsumerWarps = 8;
 
-// Vectors per thread for a row of `nvec` 16-byte vectors, and the largest
-// consumer-warp count used with it.  The cap keeps (warps + producer) low
-// enough that each SM sub-partition can give every thread the registers the
-// VPT variant needs: 17 warps -> 96 regs, 13 -> 128, 9 -> 168.
-ADALN_HD constexpr int max_consumer_warps(int vpt) {
-  return vpt == 1 ? 16 : (vpt == 2 ? 12 : 8);
+// Compiled variants of the staging kernels, chosen by the row length in
+// 16-byte vectors (nvec): vectors per thread (VPT), the largest consumer-warp
+// count, and the CTAs per SM the register budget is sized for.  At most 8
+// consumer warps share a row, so the per-row reduction work (shuffles, one
+// shared-memory exchange, scalar statistics) is repeated by few warps.  The
+// register cap follows from the warps per SM sub-partition: 14 warps per SM
+// (7 x 2 CTAs) allow 128 registers a thread, 12 or 9 warps allow 168.
+//   variant 0: nvec <=  192  VPT 1, <= 6 warps, 2 CTAs/SM
+//   variant 1: nvec <=  384  VPT 2, <= 6 warps, 2 CTAs/SM
+//   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 CTAs/SM
+//   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 CTA/SM
+ADALN_HD inline int choose_variant(int nvec) {
+  return nvec <= 192 ? 0 : (nvec <= 384 ? 1 : (nvec <= 640 ? 2 : 3));
 }
-ADALN_HD constexpr int max_threads(int vpt) {
-  return (max_consumer_warps(vpt) + 1) * 32;
-}
-ADALN_HD inline int choose_vpt(int nvec) {
-  return nvec <= 32 * max_consumer_warps(1) ? 1
-         : (nvec <= 64 * max_consumer_warps(2) ? 2 : 4);
-}
+ADALN_HD constexpr int variant_vpt(int v) { return v == 0 ? 1 : (v == 1 ? 2 : 4); }
+ADALN_HD constexpr int variant_max_warps(int v) { return v == 2 ? 5 : (v == 3 ? 8 : 6); }
+ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : 2; }
+ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
 
 struct Shape {
+  int variant;    // compiled variant (choose_variant)
   int vpt;        // 16-byte vectors per thread per row (1, 2 or 4)
   int nc;         // consumer warps
   int threads;    // (nc + 1) * 32: consumers plus one producer warp
@@ -58,6 +66,7 @@ struct FwdArgs {
   int32_t D;
   int32_t nseg;
   float eps;
+  float inv_d;  // 1 / D rounded to fp32
   unsigned* status;
 };
 
@@ -72,9 +81,11 @@ struct BwdArgs {
   float* dshift;
   float* dscale;
   float* partials;  // [G + nseg - 1][2][D] fp32: (dscale, dshift) partials
+  int32_t* seg_start;  // [nseg + 1]: first row of each segment (T at the end)
   int64_t T;
   int32_t D;
   int32_t nseg;
+  float inv_d;  // 1 / D rounded to fp32
   unsigned* status;
 };
 
@@ -86,6 +97,14 @@ cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s);
 // Number of fp32 partial slots of the backward: G + nseg - 1.
 inline int64_t bwd_slots(const Shape& s, int32_t nseg) {
   return (int64_t)s.grid + nseg - 1;
+}
+
+// Backward workspace: the partial slots, then the segment start table.
+inline size_t bwd_partials_bytes(const Shape& s, int32_t D, int32_t nseg) {
+  return (size_t)bwd_slots(s, nseg) * 2 * (size_t)D * sizeof(float);
+}
+inline size_t bwd_workspace_bytes(const Shape& s, int32_t D, int32_t nseg) {
+  return bwd_partials_bytes(s, D, nseg) + ((size_t)nseg + 1) * sizeof(int32_t);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,

@@ -3,8 +3,9 @@
 // A CTA = nc consumer warps + 1 producer warp.  The producer (one lane)
 // streams chunks of R consecutive rows from global memory into S ring stages
 // with bulk asynchronous copies, each completing on the stage's "full"
-// mbarrier; consumer warps release a stage on its "empty" mbarrier as soon as
-// they have moved its contents into registers.  Consumer thread j owns the
+// mbarrier; consumer warps read the rows from shared memory as often as
+// their passes need and release the stage on its "empty" mbarrier when they
+// are done with it.  Consumer thread j owns the
 // 16-byte column vectors j, j + 32 nc, ... of every row, so column state
 // (modulation vectors, gradient accumulators) stays in its registers for the
 // whole row range, and row sums are finished with a warp butterfly plus one
@@ -128,15 +129,18 @@ __device__ __forceinline__ bool team_sum(float (&v)[R][K], bool ok,
     okf[w] = warp_ok ? 1 : 0;
   }
   named_barrier_sync(1, nc * 32);
-  const bool mine = lane < nc;
-  bool all_ok = __all_sync(0xffffffffu, mine ? okf[lane] != 0 : true);
+  // nc <= 8: every group of 8 lanes reduces the nc warp sums (the same
+  // values in the same order), so all lanes end with identical bits.
+  const int src = lane & 7;
+  const bool mine = src < nc;
+  bool all_ok = __all_sync(0xffffffffu, mine ? okf[src] != 0 : true);
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int q = 0; q < K; ++q) {
-      float a = mine ? red[(lane * kRowsPerRound + r) * 2 + q] : 0.0f;
+      float a = mine ? red[(src * kRowsPerRound + r) * 2 + q] : 0.0f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      for (int o = 4; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
       v[r][q] = a;
     }
   return all_ok;

@@ -56,21 +56,24 @@ def test_mmdit_joint_sites(adaln):
 
 
 EDGE = [
-    # (T, D, nseg, dtype, lengths)
+    # (T, D, nseg, dtype, lengths); nvec = 16-byte vectors per row
     (1, 64, 1, "bf16", None),
     (1, 4, 1, "f32", None),
     (7, 8, 3, "bf16", [0, 7, 0]),          # T below the grid; empty first/last segment
     (1001, 136, 5, "bf16", None),          # ragged: odd T, nvec = 17
     (999, 24, 4, "f32", [1, 1, 1, 996]),   # one-row segments, nvec = 6
-    (300, 4096, 2, "bf16", None),          # nvec 512: VPT 1, 16 consumer warps
-    (300, 4104, 2, "bf16", None),          # nvec 513: VPT 2
-    (260, 6144, 3, "bf16", None),          # nvec 768: VPT 2, 12 consumer warps
-    (260, 6152, 3, "bf16", None),          # nvec 769: VPT 4
-    (200, 8192, 2, "bf16", None),          # largest bf16 row
+    (300, 1536, 2, "bf16", None),          # nvec 192: variant 0 (VPT 1), 6 warps
+    (300, 1544, 2, "bf16", None),          # nvec 193: variant 1 (VPT 2), 4 warps, ragged
+    (300, 3072, 3, "bf16", None),          # nvec 384: variant 1, 6 warps
+    (300, 3080, 3, "bf16", None),          # nvec 385: variant 2 (VPT 4), 4 warps, ragged
+    (260, 5120, 3, "bf16", None),          # nvec 640: variant 2, 5 warps
+    (260, 5128, 3, "bf16", None),          # nvec 641: variant 3 (VPT 4), 6 warps, ragged
+    (200, 8192, 2, "bf16", None),          # nvec 1024: largest bf16 row, 8 warps
     (200, 4096, 2, "f32", None),           # largest fp32 row
-    (200, 2056, 2, "f32", None),           # fp32 nvec 514: VPT 2
+    (200, 1540, 2, "f32", None),           # fp32 nvec 385: variant 2, ragged
     (2048, 1536, 2048, "bf16", [1] * 2048),  # every row its own segment
     (3000, 256, 700, "bf16", None),        # many segments, many empty
+    (4099, 512, 1, "bf16", None),          # one segment across every CTA
 ]
 
 
@@ -200,7 +203,7 @@ def test_workspace_and_alignment_errors(adaln):
     seg = torch.zeros(T, device=dev, dtype=torch.int32)
     y, m, r = adaln.adaln_fwd(x, sh, sh, seg, 1e-6)
     need = adaln.adaln_bwd_workspace_size(T, D, nseg, torch.bfloat16)
-    small = torch.empty(need - 16, device=dev, dtype=torch.uint8)
+    small = torch.empty(need - 256, device=dev, dtype=torch.uint8)  # sizes round up by < 256
     with pytest.raises(adaln.AdalnError) as e:
         adaln.adaln_bwd(x, x, m, r, sh, seg, workspace=small)
     assert e.value.code == adaln.ADALN_ERR_WORKSPACE
@@ -225,7 +228,11 @@ def test_trace_counts_launches(adaln):
 
 def test_launch_shape_matches_the_rules(adaln):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # D = 5120 bf16: 640 vectors, 4 per thread -> 5 consumer warps + 1 producer.
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 32760, 5120, 1, torch.bfloat16)
-    assert s["threads"] == 11 * 32 and s["grid"] % sms == 0 and s["stages"] >= 2
+    assert s["threads"] == 6 * 32 and s["grid"] % sms == 0 and s["stages"] >= 2
+    # D = 1536 bf16: 192 vectors, 1 per thread -> 6 consumer warps.
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 8192, 1536, 2, torch.bfloat16)
+    assert s["threads"] == 7 * 32 and s["grid"] % sms == 0
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 5, 5120, 1, torch.bfloat16)
     assert s["grid"] == 5
