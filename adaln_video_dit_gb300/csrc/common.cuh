@@ -50,6 +50,12 @@ struct F32 {
   }
 };
 
+// Compile-time flag carried into generic lambdas.
+template <bool B>
+struct Tag {
+  static constexpr bool value = B;
+};
+
 // Packed fp32x2 arithmetic (one instruction per pair on sm_100 and later).
 __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }

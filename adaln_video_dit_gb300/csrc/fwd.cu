@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
 #pragma unroll
   for (int r = 0; r < R; ++r) n_sg[r] = r < nrows ? __ldg(a.seg + r0 + r) : 0;
 
+  // Every thread's vectors are all in the row when nvec is a multiple of the
+  // consumer thread count times VPT (true for D = 1536, 3072, 5120 bf16).
+  const bool all_valid = nvec == NT * VPT;
+
   for (int64_t k = 0; k < nchunks; ++k) {
     const int s = (int)(k % stages);
     const uint32_t par = (uint32_t)((k / stages) & 1);
@@ -83,101 +87,117 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
     const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
     const uint32_t st0 = ring0 + s * stage_bytes;
 
-    // Pass 1: row sums -> mean.
-    float acc[R][1];
+    // One round over the chunk's rows.  FULL (all R rows present, every
+    // vector of this thread in the row, pipeline ok) drops the per-row and
+    // per-vector guards, so the rows' work interleaves freely.
+    auto round = [&](auto full_tag) -> bool {
+      constexpr bool FULL = decltype(full_tag)::value;
+      // Pass 1: row sums -> mean.
+      float acc[R][1];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (ok && r < rows) {
+      for (int r = 0; r < R; ++r) {
+        float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if (FULL || (ok && r < rows)) {
 #pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          if (valid[q]) {
-            float2 f[H];
-            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
+          for (int q = 0; q < VPT; ++q) {
+            if (FULL || valid[q]) {
+              float2 f[H];
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
 #pragma unroll
-            for (int e = 0; e < H; ++e) t[e & 1] = add2(t[e & 1], f[e]);
+              for (int e = 0; e < H; ++e) t[e & 1] = add2(t[e & 1], f[e]);
+            }
+          }
+        }
+        t[0] = add2(t[0], t[1]);
+        acc[r][0] = t[0].x + t[0].y;
+      }
+      if (!team_sum<R, 1>(acc, ok, rg, nc, phase)) return false;
+      phase ^= 1;
+      float mu[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) mu[r] = acc[r][0] * a.inv_d;
+
+      // Pass 2: centred sum of squares -> rstd.
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float2 nm = splat2(-mu[r]);
+        float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if (FULL || r < rows) {
+#pragma unroll
+          for (int q = 0; q < VPT; ++q) {
+            if (FULL || valid[q]) {
+              float2 f[H];
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
+#pragma unroll
+              for (int e = 0; e < H; ++e) {
+                const float2 c = add2(f[e], nm);
+                t[e & 1] = fma2(c, c, t[e & 1]);
+              }
+            }
+          }
+        }
+        t[0] = add2(t[0], t[1]);
+        acc[r][0] = t[0].x + t[0].y;
+      }
+      team_sum<R, 1>(acc, true, rg, nc, phase);
+      phase ^= 1;
+
+      // Segment bookkeeping for the chunk's rows, then the modulated outputs.
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (FULL || r < rows) {
+          const int b = checked_seg(sg[r], prev_b, a.nseg, a.status);
+          prev_b = b;
+          sg[r] = b;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (FULL || r < rows) {
+          const int64_t t = t0 + r;
+          const float rs = rsqrtf(fmaf(acc[r][0], a.inv_d, a.eps));
+          const int b = sg[r];
+          if (b != cur_b) {
+            cur_b = b;
+#pragma unroll
+            for (int q = 0; q < VPT; ++q) {
+              if (valid[q]) {
+                const size_t off = ((size_t)b * nvec + j + q * NT) * 16;
+                E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.scale) + off), s1[q]);
+                E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.shift) + off), sh[q]);
+#pragma unroll
+                for (int e = 0; e < H; ++e) s1[q][e] = add2(s1[q][e], splat2(1.0f));
+              }
+            }
+          }
+          const float2 nm = splat2(-mu[r]), rs2 = splat2(rs);
+#pragma unroll
+          for (int q = 0; q < VPT; ++q) {
+            if (FULL || valid[q]) {
+              const int v = j + q * NT;
+              float2 f[H];
+              E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), f);
+#pragma unroll
+              for (int e = 0; e < H; ++e) f[e] = fma2(mul2(add2(f[e], nm), rs2), s1[q][e], sh[q][e]);
+              st_global_cs_v4(static_cast<unsigned char*>(a.y) + ((size_t)t * nvec + v) * 16,
+                              E::pack2(f));
+            }
+          }
+          if (j == 0) {
+            a.mean[t] = mu[r];
+            a.rstd[t] = rs;
           }
         }
       }
-      t[0] = add2(t[0], t[1]);
-      acc[r][0] = t[0].x + t[0].y;
-    }
-    if (!team_sum<R, 1>(acc, ok, rg, nc, phase)) {
+      return true;
+    };
+    const bool full = ok && rows == R && all_valid;
+    if (!(full ? round(Tag<true>()) : round(Tag<false>()))) {
       if (j == 0) {
         atomicOr(a.status, ADALN_DEV_TIMEOUT);
         *rg.abort = 1;
       }
       break;
-    }
-    phase ^= 1;
-    float mu[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) mu[r] = acc[r][0] * a.inv_d;
-
-    // Pass 2: centred sum of squares -> rstd.
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float2 nm = splat2(-mu[r]);
-      float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (r < rows) {
-#pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          if (valid[q]) {
-            float2 f[H];
-            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + j + q * NT) * 16), f);
-#pragma unroll
-            for (int e = 0; e < H; ++e) {
-              const float2 c = add2(f[e], nm);
-              t[e & 1] = fma2(c, c, t[e & 1]);
-            }
-          }
-        }
-      }
-      t[0] = add2(t[0], t[1]);
-      acc[r][0] = t[0].x + t[0].y;
-    }
-    team_sum<R, 1>(acc, true, rg, nc, phase);
-    phase ^= 1;
-
-    // Modulate and store.
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (r < rows) {
-        const int64_t t = t0 + r;
-        const float rs = rsqrtf(fmaf(acc[r][0], a.inv_d, a.eps));
-        const int b = checked_seg(sg[r], prev_b, a.nseg, a.status);
-        prev_b = b;
-        if (b != cur_b) {
-          cur_b = b;
-#pragma unroll
-          for (int q = 0; q < VPT; ++q) {
-            if (valid[q]) {
-              const size_t off = ((size_t)b * nvec + j + q * NT) * 16;
-              E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.scale) + off), s1[q]);
-              E::unpack2(ld_global_v4(static_cast<const unsigned char*>(a.shift) + off), sh[q]);
-#pragma unroll
-              for (int e = 0; e < H; ++e) s1[q][e] = add2(s1[q][e], splat2(1.0f));
-            }
-          }
-        }
-        const float2 nm = splat2(-mu[r]), rs2 = splat2(rs);
-#pragma unroll
-        for (int q = 0; q < VPT; ++q) {
-          if (valid[q]) {
-            const int v = j + q * NT;
-            float2 f[H];
-            E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), f);
-#pragma unroll
-            for (int e = 0; e < H; ++e) f[e] = fma2(mul2(add2(f[e], nm), rs2), s1[q][e], sh[q][e]);
-            st_global_cs_v4(static_cast<unsigned char*>(a.y) + ((size_t)t * nvec + v) * 16,
-                            E::pack2(f));
-          }
-        }
-        if (j == 0) {
-          a.mean[t] = mu[r];
-          a.rstd[t] = rs;
-        }
-      }
     }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
