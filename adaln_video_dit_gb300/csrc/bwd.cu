@@ -227,14 +227,16 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
       }
       phase ^= 1;
 
-      // Phase 2: dx = rstd (g - mean g - xhat mean(g xhat)).
+      // Phase 2: dx = rstd (g - mean g - xhat mean(g xhat)), rearranged as
+      //   dx = dy (rstd (1 + scale)) + (x - mean) k1 + k0,
+      //   k1 = -rstd^2 mean(g xhat),  k0 = -rstd mean(g).
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         if (r >= lo && r < hi) {
           const int64_t t = r0 + k * R + r;
           const float2 nm = splat2(-cmu[r]), r2 = splat2(crs[r]);
-          const float2 nmg = splat2(-part[r][0] * a.inv_d);
-          const float2 nmgx = splat2(-part[r][1] * a.inv_d);
+          const float2 k0 = splat2(-crs[r] * (part[r][0] * a.inv_d));
+          const float2 k1 = splat2(-(crs[r] * crs[r]) * (part[r][1] * a.inv_d));
 #pragma unroll
           for (int q = 0; q < VPT; ++q) {
             if (valid[q]) {
@@ -243,11 +245,8 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
               E::unpack2(ld_shared_v4(st0 + (uint32_t)(r * nvec + v) * 16), fx);
               E::unpack2(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
 #pragma unroll
-              for (int e = 0; e < H; ++e) {
-                const float2 xh = mul2(add2(fx[e], nm), r2);
-                const float2 g = mul2(fd[e], s1[q][e]);
-                fx[e] = mul2(fma2(xh, nmgx, add2(g, nmg)), r2);
-              }
+              for (int e = 0; e < H; ++e)
+                fx[e] = fma2(fd[e], mul2(s1[q][e], r2), fma2(add2(fx[e], nm), k1, k0));
               st_global_cs_v4(static_cast<unsigned char*>(a.dx) + ((size_t)t * nvec + v) * 16,
                               E::pack2(fx));
             }
