@@ -26,7 +26,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ["adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_noalloc",
            "adaln_get_status", "adaln_strerror", "adaln_trace_begin",
-           "adaln_trace_end", "adaln_trace_get", "adaln_launch_shape"]
+           "adaln_trace_end", "adaln_trace_get", "adaln_launch_shape",
+           "adaln_selftest_wait_timeout"]
 
 
 class AdalnError(RuntimeError):
@@ -63,6 +64,8 @@ def _load():
     lib.adaln_trace_get.restype = ci
     lib.adaln_trace_get.argtypes = [ci, ctypes.POINTER(ctypes.c_int64),
                                     ctypes.POINTER(ctypes.c_double)]
+    lib.adaln_selftest_wait_timeout.restype = ci
+    lib.adaln_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     lib.adaln_launch_shape.restype = ci
     lib.adaln_launch_shape.argtypes = [ci, i64, i32, i32, ci] + [ctypes.POINTER(i32)] * 4
     return lib
@@ -227,6 +230,13 @@ def adaln_trace_get(kernel_id):
     _check(raw.adaln_trace_get(int(kernel_id), ctypes.byref(n), ctypes.byref(ms)),
            "adaln_trace_get")
     return n.value, ms.value
+
+
+def adaln_selftest_wait_timeout(limit_us, stream=None):
+    """Launch the bounded-wait self-test (see include/adaln.h)."""
+    dev = torch.cuda.current_device()
+    _check(raw.adaln_selftest_wait_timeout(int(limit_us), _stream_ptr(stream, dev)),
+           "adaln_selftest_wait_timeout")
 
 
 def adaln_launch_shape(which, T, D, nseg, dtype):

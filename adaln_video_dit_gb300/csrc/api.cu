@@ -293,6 +293,16 @@ int adaln_trace_get(int kernel_id, int64_t* launches, double* total_ms) {
   return ADALN_OK;
 }
 
+int adaln_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 100000) return ADALN_ERR_ARG;
+  unsigned* status = nullptr;
+  cudaError_t e = status_ptr(&status);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_wait_timeout_probe(status, (uint64_t)limit_us * 1000ull,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
+}
+
 int adaln_launch_shape(int which, int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype,
                        int32_t* grid, int32_t* threads, int32_t* stages, int32_t* smem_bytes) {
   int rc = check_dims(T, D, nseg, dtype);

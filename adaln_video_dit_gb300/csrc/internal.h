@@ -114,6 +114,9 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt,
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s,
                                 cudaStream_t st);
 
+// Bounded-wait self-test (selftest.cu).
+cudaError_t launch_wait_timeout_probe(unsigned* status, uint64_t limit_ns, cudaStream_t st);
+
 // Shared-memory header of the staging kernels (barriers, flags, reduction
 // scratch), before the 128-byte aligned ring.
 ADALN_HD inline int ring_header_bytes(int stages) {

@@ -46,6 +46,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--report", choices=["unfused"], default=None,
+                   help="instead of the benchmark line: compare with torch's unfused "
+                        "chain (time and saved activation bytes)")
     return p.parse_args()
 
 
@@ -446,8 +449,114 @@ def load_traffic(kernel):
         return None, "no ncu capture"
 
 
+# ---------------------------------------------------------------------------
+# Context report: torch's unfused chain (layer_norm, gather, multiply, add and
+# their autograd backward) against the fused operator on the same inputs.
+# ---------------------------------------------------------------------------
+def report_unfused(args):
+    import torch
+    import torch.nn.functional as F
+    from adaln_video_dit_gb300 import _lib as L
+    from adaln_video_dit_gb300 import autograd as A
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, device=dev, dtype=torch.float32)
+    flush_out = torch.empty((), device=dev, dtype=torch.float32)
+
+    def timed(fn, reps=30, warm=5):
+        for _ in range(warm):
+            fn()
+        ms = []
+        for _ in range(reps):
+            torch.sum(flush, dim=0, out=flush_out)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    def saved_bytes(fn):
+        seen = {}
+
+        def pack(t):
+            st = t.untyped_storage()
+            seen[st.data_ptr()] = max(seen.get(st.data_ptr(), 0), st.nbytes())
+            return t
+        with torch.autograd.graph.saved_tensors_hooks(pack, lambda t: t):
+            fn()
+        return sum(seen.values())
+
+    out = {"report": "unfused_torch_vs_fused", "device": torch.cuda.get_device_name(dev),
+           "torch": torch.__version__, "dtype": "bf16", "l2": "evicted by a 2x L2 read before each rep",
+           "cases": []}
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    for name, T, D in (("long_video", 32760, 5120), ("N=64000", 64000, 5120)):
+        x = torch.randn(T, D, device=dev, generator=g).to(torch.bfloat16)
+        dy = (torch.randn(T, D, device=dev, generator=g) * 1e-2).to(torch.bfloat16)
+        shift = (torch.randn(1, D, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+        scale = (torch.randn(1, D, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+        seg = torch.zeros(T, device=dev, dtype=torch.int32)
+        y, mean, rstd = L.adaln_fwd(x, shift, scale, seg, 1e-6)
+        dx = torch.empty_like(x)
+        dsh = torch.empty(1, D, device=dev)
+        dsc = torch.empty(1, D, device=dev)
+        ws = torch.empty(L.adaln_bwd_workspace_size(T, D, 1, torch.bfloat16), device=dev,
+                         dtype=torch.uint8)
+
+        def fused_fwd():
+            L.adaln_fwd(x, shift, scale, seg, 1e-6, y=y, mean=mean, rstd=rstd)
+
+        def fused_fwd_bwd():
+            fused_fwd()
+            L.adaln_bwd(dy, x, mean, rstd, scale, seg, dx=dx, dshift=dsh, dscale=dsc, workspace=ws)
+
+        # The usual DiT form of the unfused chain: per-sample modulation
+        # broadcast over the sample's tokens ([B, N, D] with [B, 1, D]; B = 1).
+        def unfused_fwd():
+            with torch.no_grad():
+                xb = x.view(1, T, D)
+                F.layer_norm(xb, (D,), eps=1e-6) * (1 + scale.view(1, 1, D)) + shift.view(1, 1, D)
+
+        xg = x.detach().requires_grad_(True)
+        shg = shift.detach().requires_grad_(True)
+        scg = scale.detach().requires_grad_(True)
+
+        def unfused_chain():
+            xb = xg.view(1, T, D)
+            return (F.layer_norm(xb, (D,), eps=1e-6) * (1 + scg.view(1, 1, D))
+                    + shg.view(1, 1, D))
+
+        def unfused_fwd_bwd():
+            unfused_chain().backward(dy.view(1, T, D))
+
+        t_ff, t_ffb = timed(fused_fwd), timed(fused_fwd_bwd)
+        t_uf, t_ufb = timed(unfused_fwd), timed(unfused_fwd_bwd)
+        fused_saved = saved_bytes(lambda: A.adaln_modulate(xg, shg, scg, seg))
+        chain_saved = saved_bytes(unfused_chain)
+        out["cases"].append({
+            "workload": name, "T": T, "D": D,
+            "fused_fwd_ms": t_ff, "fused_fwd_bwd_ms": t_ffb,
+            "unfused_fwd_ms": t_uf, "unfused_fwd_bwd_ms": t_ufb,
+            "speedup_fwd": t_uf / t_ff, "speedup_bwd": (t_ufb - t_uf) / (t_ffb - t_ff),
+            "speedup_fwd_bwd": t_ufb / t_ffb,
+            "saved_bytes_fused": fused_saved, "saved_bytes_unfused": chain_saved,
+            "activation_memory_saving": 1.0 - fused_saved / chain_saved})
+        del x, dy, y, dx, xg, ws
+        torch.cuda.empty_cache()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.report == "unfused":
+        report_unfused(args)
+        return
     rank, local, world, pg = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -179,6 +179,16 @@ ADALN_API int adaln_trace_end(void);
 ADALN_API int adaln_trace_get(int kernel_id, int64_t* launches, double* total_ms);
 
 /*
+ * Self-test of failure detection: launches one thread that waits, through the
+ * bounded wait the staging pipelines use, on an mbarrier that nothing ever
+ * completes, giving up after limit_us microseconds (1..100000).  On return of
+ * the next adaln_get_status() the device status word must hold
+ * ADALN_DEV_TIMEOUT (ADALN_ERR_TIMEOUT), and the device must remain usable.
+ * The pipelines' own limit is 2 s; the staging kernels never wait unbounded.
+ */
+ADALN_API int adaln_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
+/*
  * Launch shape chosen for these sizes on the current device: grid (CTAs),
  * threads per CTA, ring stages, dynamic shared memory bytes.  `which` is
  * ADALN_KERNEL_FWD or ADALN_KERNEL_BWD_ROWS.  For reports and tests.

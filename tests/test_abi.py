@@ -112,6 +112,11 @@ def test_trace_argument_checks(lib):
     assert n.value == 0 and ms.value == 0.0
 
 
+def test_selftest_limit_is_checked_on_host(lib):
+    assert lib.raw.adaln_selftest_wait_timeout(0, None) == lib.ADALN_ERR_ARG
+    assert lib.raw.adaln_selftest_wait_timeout(100001, None) == lib.ADALN_ERR_ARG
+
+
 def test_binding_rejects_host_tensors(lib):
     import torch
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
