@@ -276,24 +276,26 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
     for (int b = prev_last + 1 + j; b <= a.nseg; b += NT) a.seg_start[b] = (int32_t)a.T;
 }
 
-// Sum the partials of each segment in CTA order.  Block (b, column block of
-// 8 float4 columns) has J warps; lane l handles column (l & 7) of the block
-// and slot group g = 4 w + (l >> 3) of 4J groups, each a contiguous run of
-// the segment's CTAs summed in order; thread group g = 0 then adds the 4J
-// group sums in group order.  The order of every sum is fixed by (T, G,
-// nseg), so results are bitwise reproducible.  Launched as a programmatic
-// dependent of the row pass: it waits (griddepcontrol.wait) until the row
-// pass has completed and its writes are visible.
-constexpr int kFinalizeMaxWarps = 8;
+// Sum the partials of each segment in CTA order.  A slot holds 2D floats
+// (dscale partial, then dshift partial), read as 2D/4 float4 columns.  Block
+// (b, column block of 8 float4 columns) has J warps; lane l handles column
+// (l & 7) of the block and slot group g = 4 w + (l >> 3) of 4J groups, each a
+// contiguous run of the segment's CTAs summed in order (up to 8 slots' loads
+// in flight at a time); the first 8 threads then add the 4J group sums in
+// group order.  The order of every sum is fixed by (T, G, nseg), so results
+// are bitwise reproducible.  Launched as a programmatic dependent of the row
+// pass: it waits (griddepcontrol.wait) until the row pass has completed and
+// its writes are visible.
+constexpr int kFinalizeMaxWarps = 12;
 
-__global__ void __launch_bounds__(32 * kFinalizeMaxWarps)
+__global__ void __launch_bounds__(32 * kFinalizeMaxWarps, 2)
     adaln_bwd_finalize_kernel(BwdArgs a, int G, int J) {
-  __shared__ float4 sh_s[4 * kFinalizeMaxWarps][8], sh_b[4 * kFinalizeMaxWarps][8];
+  __shared__ float4 sh[4 * kFinalizeMaxWarps][8];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int ncol4 = a.D / 4;
-  const int col4 = blockIdx.y * 8 + (lane & 7);
+  const int ncol4 = a.D / 4;             // float4 columns of one half
+  const int col4 = blockIdx.y * 8 + (lane & 7);  // in [0, 2 ncol4)
   const int g = 4 * w + (lane >> 3), ng = 4 * J;
 
   // Rows of segment b: [seg_start[b], seg_start[b + 1]), recorded by the
@@ -306,47 +308,38 @@ __global__ void __launch_bounds__(32 * kFinalizeMaxWarps)
     sb = sb < 0 ? 0 : (sb > a.T ? a.T : sb);
     eb = eb < 0 ? 0 : (eb > a.T ? a.T : eb);
   }
-  float4 ps = make_float4(0.f, 0.f, 0.f, 0.f), pb = ps;
-  if (eb > sb && col4 < ncol4) {
+  float4 ps = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (eb > sb && col4 < 2 * ncol4) {
     const int64_t c0 = part_owner(sb, a.T, G), c1 = part_owner(eb - 1, a.T, G);
     const int64_t n = c1 - c0 + 1;
     const int64_t lo = c0 + (n * g) / ng, hi = c0 + (n * (g + 1)) / ng;
-    const size_t row4 = 2 * (size_t)a.D / 4;  // float4 per slot
+    const size_t row4 = 2 * (size_t)ncol4;  // float4 per slot
     const float4* base = reinterpret_cast<const float4*>(a.partials) + col4;
-    int64_t c = lo;
-    for (; c + 4 <= hi; c += 4) {
-      float4 u[4], v[4];
+    for (int64_t c = lo; c < hi; c += 8) {
+      float4 u[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4* p = base + (size_t)(c + i + b) * row4;
-        u[i] = __ldcs(p);
-        v[i] = __ldcs(p + ncol4);
-      }
+      for (int i = 0; i < 8; ++i)
+        if (c + i < hi) u[i] = __ldcs(base + (size_t)(c + i + b) * row4);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ps.x += u[i].x; ps.y += u[i].y; ps.z += u[i].z; ps.w += u[i].w;
-        pb.x += v[i].x; pb.y += v[i].y; pb.z += v[i].z; pb.w += v[i].w;
+      for (int i = 0; i < 8; ++i) {
+        if (c + i < hi) {
+          ps.x += u[i].x; ps.y += u[i].y; ps.z += u[i].z; ps.w += u[i].w;
+        }
       }
-    }
-    for (; c < hi; ++c) {
-      const float4* p = base + (size_t)(c + b) * row4;
-      const float4 u = __ldcs(p), v = __ldcs(p + ncol4);
-      ps.x += u.x; ps.y += u.y; ps.z += u.z; ps.w += u.w;
-      pb.x += v.x; pb.y += v.y; pb.z += v.z; pb.w += v.w;
     }
   }
-  sh_s[g][lane & 7] = ps;
-  sh_b[g][lane & 7] = pb;
+  sh[g][lane & 7] = ps;
   __syncthreads();
-  if (threadIdx.x < 8 && col4 < ncol4) {
-    float4 ts = sh_s[0][lane], tb = sh_b[0][lane];
+  if (threadIdx.x < 8 && col4 < 2 * ncol4) {
+    float4 ts = sh[0][lane];
     for (int i = 1; i < ng; ++i) {
-      const float4 u = sh_s[i][lane], v = sh_b[i][lane];
+      const float4 u = sh[i][lane];
       ts.x += u.x; ts.y += u.y; ts.z += u.z; ts.w += u.w;
-      tb.x += v.x; tb.y += v.y; tb.z += v.z; tb.w += v.w;
     }
-    reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D)[col4] = ts;
-    reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D)[col4] = tb;
+    if (col4 < ncol4)
+      reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D)[col4] = ts;
+    else
+      reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D)[col4 - ncol4] = ts;
   }
 }
 
@@ -390,16 +383,16 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
 }
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {
-  // Warps per block: about 8 partials per slot group for a segment spanning
+  // Warps per block: about 6 partials per slot group for a segment spanning
   // all CTAs, a single warp when many segments share the CTAs.
   const int64_t per_seg = ((int64_t)s.grid + a.nseg - 1) / a.nseg;
-  int J = (int)((per_seg + 31) / 32);
+  int J = (int)((per_seg + 23) / 24);
   J = J < 1 ? 1 : (J > kFinalizeMaxWarps ? kFinalizeMaxWarps : J);
   int G = s.grid;
   BwdArgs args = a;
   void* params[] = {&args, &G, &J};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((a.D / 4 + 7) / 8));
+  cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((2 * (a.D / 4) + 7) / 8));
   cfg.blockDim = dim3(32 * J);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
