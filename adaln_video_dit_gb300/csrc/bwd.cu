@@ -68,10 +68,17 @@ __device__ __forceinline__ void flush_partials(float* partials, int64_t slot, in
 // registers) and the flush of the run's partial between runs.  A chunk that
 // a segment boundary splits is visited once per run, each visit handling its
 // rows of that run; its stage is released after the last visit.
-template <class E, int VARIANT, int R>
+// EXACT: the row fills the variant's largest consumer-warp count exactly
+// (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
+// the warp count and row length are compile-time constants (offsets fold
+// into immediates, no per-vector guards).
+template <class E, int VARIANT, int R, bool EXACT>
 __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
-    adaln_bwd_rows_kernel(BwdArgs a, int nc, int stages, int nvec) {
+    adaln_bwd_rows_kernel(BwdArgs a, int nc_rt, int stages, int nvec_rt) {
   constexpr int VPT = variant_vpt(VARIANT);
+  constexpr int NC_X = variant_max_warps(VARIANT);
+  const int nc = EXACT ? NC_X : nc_rt;
+  const int nvec = EXACT ? NC_X * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;
   extern __shared__ __align__(128) unsigned char smem[];
   // Let the finalize grid be scheduled as soon as SMs free up; it waits for
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
   const uint32_t stage_bytes = (uint32_t)R * row_bytes * 2;
   bool valid[VPT];
 #pragma unroll
-  for (int q = 0; q < VPT; ++q) valid[q] = j + q * NT < nvec;
+  for (int q = 0; q < VPT; ++q) valid[q] = EXACT || j + q * NT < nvec;
 
   float2 acc_s[VPT][H], acc_b[VPT][H], s1[VPT][H];
   int s1_seg = -1;  // segment whose (1 + scale) is in s1
@@ -351,31 +358,38 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 
 namespace {
 
+template <class E, int V>
+void* rows_kernel_for_v(bool exact) {
+  return exact ? reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, kBwdRows, true>)
+               : reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, kBwdRows, false>);
+}
+
 template <class E>
-void* rows_kernel_for(int variant) {
+void* rows_kernel_for(int variant, bool exact) {
   switch (variant) {
-    case 0: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 0, kBwdRows>);
-    case 1: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 1, kBwdRows>);
-    case 2: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 2, kBwdRows>);
-    default: return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, 3, kBwdRows>);
+    case 0: return rows_kernel_for_v<E, 0>(exact);
+    case 1: return rows_kernel_for_v<E, 1>(exact);
+    case 2: return rows_kernel_for_v<E, 2>(exact);
+    default: return rows_kernel_for_v<E, 3>(exact);
   }
 }
 
-void* pick_rows(adaln_dtype_t dt, int variant) {
-  return dt == ADALN_BF16 ? rows_kernel_for<BF16>(variant) : rows_kernel_for<F32>(variant);
+void* pick_rows(adaln_dtype_t dt, int variant, bool exact) {
+  return dt == ADALN_BF16 ? rows_kernel_for<BF16>(variant, exact) : rows_kernel_for<F32>(variant, exact);
 }
 
 }  // namespace
 
 cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
-  const int variant = choose_variant(D * esize / 16);
-  return staging_shape(pick_rows(dt, variant), T, D, dt, 2, kBwdRows, s);
+  const int nvec = D * esize / 16;
+  return staging_shape(pick_rows(dt, choose_variant(nvec), variant_exact(nvec)), T, D, dt, 2,
+                       kBwdRows, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
                             cudaStream_t st) {
-  void* k = pick_rows(dt, s.variant);
+  void* k = pick_rows(dt, s.variant, s.exact);
   int nc = s.nc, stages = s.stages, nvec = s.nvec;
   BwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec};

@@ -137,6 +137,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // bit and an orderly exit instead of a hang.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// As mbar_try_wait, but the thread may be suspended (instead of spinning)
+// until the phase completes or about `hint_ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Suspend hint of the waits below: long enough that a waiting thread sleeps
+// instead of spinning (taking issue slots from the other warps), short
+// enough that the abort flag and the time bound are still polled.
+constexpr uint32_t kWaitSleepHintNs = 20000;
+
 // Wait for phase `parity` of barrier `bar` to complete.  Gives up (returns
 // false) after `limit_ns` (default kWaitLimitNs), or early once *abort is set.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
@@ -144,12 +164,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

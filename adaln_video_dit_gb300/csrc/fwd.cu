@@ -16,10 +16,17 @@
 
 namespace adaln {
 
-template <class E, int VARIANT, int R>
+// EXACT: the row fills the variant's largest consumer-warp count exactly
+// (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
+// the warp count and row length are compile-time constants (offsets fold
+// into immediates, no per-vector guards).
+template <class E, int VARIANT, int R, bool EXACT>
 __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
-    adaln_fwd_kernel(FwdArgs a, int nc, int stages, int nvec) {
+    adaln_fwd_kernel(FwdArgs a, int nc_rt, int stages, int nvec_rt) {
   constexpr int VPT = variant_vpt(VARIANT);
+  constexpr int NC_X = variant_max_warps(VARIANT);
+  const int nc = EXACT ? NC_X : nc_rt;
+  const int nvec = EXACT ? NC_X * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;  // float2 pairs per vector
   extern __shared__ __align__(128) unsigned char smem[];
   const Ring rg = ring_layout(smem, stages);
@@ -47,7 +54,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
   const uint32_t stage_bytes = (uint32_t)R * row_bytes;
   bool valid[VPT];
 #pragma unroll
-  for (int q = 0; q < VPT; ++q) valid[q] = j + q * NT < nvec;
+  for (int q = 0; q < VPT; ++q) valid[q] = EXACT || j + q * NT < nvec;
 
   // (1 + scale) and shift of the current segment for this thread's columns.
   float2 s1[VPT][H], sh[VPT][H];
@@ -67,7 +74,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
 
   // Every thread's vectors are all in the row when nvec is a multiple of the
   // consumer thread count times VPT (true for D = 1536, 3072, 5120 bf16).
-  const bool all_valid = nvec == NT * VPT;
+  const bool all_valid = EXACT || nvec == NT * VPT;
 
   for (int64_t k = 0; k < nchunks; ++k) {
     const int s = (int)(k % stages);
@@ -209,18 +216,24 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
 // ---------------------------------------------------------------------------
 namespace {
 
+template <class E, int V>
+void* fwd_kernel_for_v(bool exact) {
+  return exact ? reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, kFwdRows, true>)
+               : reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, kFwdRows, false>);
+}
+
 template <class E>
-void* fwd_kernel_for(int variant) {
+void* fwd_kernel_for(int variant, bool exact) {
   switch (variant) {
-    case 0: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 0, kFwdRows>);
-    case 1: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 1, kFwdRows>);
-    case 2: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 2, kFwdRows>);
-    default: return reinterpret_cast<void*>(&adaln_fwd_kernel<E, 3, kFwdRows>);
+    case 0: return fwd_kernel_for_v<E, 0>(exact);
+    case 1: return fwd_kernel_for_v<E, 1>(exact);
+    case 2: return fwd_kernel_for_v<E, 2>(exact);
+    default: return fwd_kernel_for_v<E, 3>(exact);
   }
 }
 
-void* pick_fwd(adaln_dtype_t dt, int variant) {
-  return dt == ADALN_BF16 ? fwd_kernel_for<BF16>(variant) : fwd_kernel_for<F32>(variant);
+void* pick_fwd(adaln_dtype_t dt, int variant, bool exact) {
+  return dt == ADALN_BF16 ? fwd_kernel_for<BF16>(variant, exact) : fwd_kernel_for<F32>(variant, exact);
 }
 
 }  // namespace
@@ -235,6 +248,7 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   s->row_bytes = D * esize;
   s->nvec = s->row_bytes / 16;
   s->variant = choose_variant(s->nvec);
+  s->exact = variant_exact(s->nvec);
   s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
   s->threads = (s->nc + 1) * 32;
@@ -289,13 +303,14 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 
 cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
-  const int variant = choose_variant(D * esize / 16);
-  return staging_shape(pick_fwd(dt, variant), T, D, dt, 1, kFwdRows, s);
+  const int nvec = D * esize / 16;
+  return staging_shape(pick_fwd(dt, choose_variant(nvec), variant_exact(nvec)), T, D, dt, 1,
+                       kFwdRows, s);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st) {
-  void* k = pick_fwd(dt, s.variant);
+  void* k = pick_fwd(dt, s.variant, s.exact);
   int nc = s.nc, stages = s.stages, nvec = s.nvec;
   FwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec};

@@ -41,9 +41,14 @@ ADALN_HD constexpr int variant_vpt(int v) { return v == 0 ? 1 : (v == 1 ? 2 : 4)
 ADALN_HD constexpr int variant_max_warps(int v) { return v == 2 ? 5 : (v == 3 ? 8 : 6); }
 ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : 2; }
 ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
+ADALN_HD inline bool variant_exact(int nvec) {
+  const int v = choose_variant(nvec);
+  return nvec == variant_max_warps(v) * 32 * variant_vpt(v);
+}
 
 struct Shape {
   int variant;    // compiled variant (choose_variant)
+  bool exact;     // nvec fills the variant's largest warp count exactly
   int vpt;        // 16-byte vectors per thread per row (1, 2 or 4)
   int nc;         // consumer warps
   int threads;    // (nc + 1) * 32: consumers plus one producer warp
