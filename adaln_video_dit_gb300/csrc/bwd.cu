@@ -284,26 +284,28 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
 }
 
 // Sum the partials of each segment in CTA order.  A slot holds 2D floats
-// (dscale partial, then dshift partial), read as 2D/4 float4 columns.  Block
-// (b, column block of 8 float4 columns) has J warps; lane l handles column
-// (l & 7) of the block and slot group g = 4 w + (l >> 3) of 4J groups, each a
-// contiguous run of the segment's CTAs summed in order (up to 8 slots' loads
-// in flight at a time); the first 8 threads then add the 4J group sums in
-// group order.  The order of every sum is fixed by (T, G, nseg), so results
-// are bitwise reproducible.  Launched as a programmatic dependent of the row
-// pass: it waits (griddepcontrol.wait) until the row pass has completed and
-// its writes are visible.
-constexpr int kFinalizeMaxWarps = 12;
+// (dscale partial, then dshift partial), read as 2D/4 float4 columns.  A block
+// of 256 threads covers CB = 256 / GPC consecutive float4 columns of one
+// segment; each column is split over GPC slot groups (contiguous runs of the
+// segment's CTAs, each summed in slot order with up to 8 loads in flight),
+// and the group sums are combined by a fixed pairwise tree.  GPC follows the
+// number of partials per segment: 1 when segments are short (each thread a
+// column, blocks span 256 columns), up to 64 for a segment spanning every CTA.
+// The order of every sum is fixed by (T, G, nseg), so results are bitwise
+// reproducible.  Launched as a programmatic dependent of the row pass: it
+// waits (griddepcontrol.wait) until the row pass has completed and its writes
+// are visible.
+constexpr int kFinalizeThreads = 256;
 
-__global__ void __launch_bounds__(32 * kFinalizeMaxWarps, 2)
-    adaln_bwd_finalize_kernel(BwdArgs a, int G, int J) {
-  __shared__ float4 sh[4 * kFinalizeMaxWarps][8];
+__global__ void __launch_bounds__(kFinalizeThreads, 4)
+    adaln_bwd_finalize_kernel(BwdArgs a, int G, int gpc) {
+  __shared__ float4 sh[kFinalizeThreads];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int ncol4 = a.D / 4;             // float4 columns of one half
-  const int col4 = blockIdx.y * 8 + (lane & 7);  // in [0, 2 ncol4)
-  const int g = 4 * w + (lane >> 3), ng = 4 * J;
+  const int cb = kFinalizeThreads / gpc;   // columns per block
+  const int ncol4 = a.D / 4;               // float4 columns of one half
+  const int cl = threadIdx.x % cb, g = threadIdx.x / cb;
+  const int col4 = blockIdx.y * cb + cl;   // in [0, 2 ncol4)
 
   // Rows of segment b: [seg_start[b], seg_start[b + 1]), recorded by the
   // row pass.  Clamped so that inconsistent input (reported in the status
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(32 * kFinalizeMaxWarps, 2)
   if (eb > sb && col4 < 2 * ncol4) {
     const int64_t c0 = part_owner(sb, a.T, G), c1 = part_owner(eb - 1, a.T, G);
     const int64_t n = c1 - c0 + 1;
-    const int64_t lo = c0 + (n * g) / ng, hi = c0 + (n * (g + 1)) / ng;
+    const int64_t lo = c0 + (n * g) / gpc, hi = c0 + (n * (g + 1)) / gpc;
     const size_t row4 = 2 * (size_t)ncol4;  // float4 per slot
     const float4* base = reinterpret_cast<const float4*>(a.partials) + col4;
     for (int64_t c = lo; c < hi; c += 8) {
@@ -335,18 +337,24 @@ __global__ void __launch_bounds__(32 * kFinalizeMaxWarps, 2)
       }
     }
   }
-  sh[g][lane & 7] = ps;
-  __syncthreads();
-  if (threadIdx.x < 8 && col4 < 2 * ncol4) {
-    float4 ts = sh[0][lane];
-    for (int i = 1; i < ng; ++i) {
-      const float4 u = sh[i][lane];
-      ts.x += u.x; ts.y += u.y; ts.z += u.z; ts.w += u.w;
+  if (gpc > 1) {
+    sh[threadIdx.x] = ps;
+    __syncthreads();
+    // Fixed pairwise tree over the groups: group g absorbs group g + h.
+    for (int h = gpc / 2; h >= 1; h >>= 1) {
+      if (g < h) {
+        const float4 u = sh[threadIdx.x + h * cb];
+        ps.x += u.x; ps.y += u.y; ps.z += u.z; ps.w += u.w;
+        sh[threadIdx.x] = ps;
+      }
+      __syncthreads();
     }
+  }
+  if (g == 0 && col4 < 2 * ncol4) {
     if (col4 < ncol4)
-      reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D)[col4] = ts;
+      reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D)[col4] = ps;
     else
-      reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D)[col4 - ncol4] = ts;
+      reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D)[col4 - ncol4] = ps;
   }
 }
 
@@ -397,17 +405,18 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
 }
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {
-  // Warps per block: about 6 partials per slot group for a segment spanning
-  // all CTAs, a single warp when many segments share the CTAs.
+  // Slot groups per column: about 4-8 partials per group for the longest
+  // segments (power of two, 1..64), a single group when segments are short.
   const int64_t per_seg = ((int64_t)s.grid + a.nseg - 1) / a.nseg;
-  int J = (int)((per_seg + 23) / 24);
-  J = J < 1 ? 1 : (J > kFinalizeMaxWarps ? kFinalizeMaxWarps : J);
+  int gpc = 1;
+  while (gpc < 64 && per_seg > 8 * gpc) gpc *= 2;
   int G = s.grid;
   BwdArgs args = a;
-  void* params[] = {&args, &G, &J};
+  void* params[] = {&args, &G, &gpc};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((2 * (a.D / 4) + 7) / 8));
-  cfg.blockDim = dim3(32 * J);
+  const int cb = kFinalizeThreads / gpc;
+  cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((2 * (a.D / 4) + cb - 1) / cb));
+  cfg.blockDim = dim3(kFinalizeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   // Programmatic dependent launch: the launch overlaps the row pass's tail;
