@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 4)
 // Host side.
 // ---------------------------------------------------------------------------
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
-                          int ntensors, int rows_per_round, Shape* s);
+                          int ntensors, int rows_per_round, int variant, Shape* s);
 
 namespace {
 
@@ -378,6 +378,7 @@ void* rows_kernel_for(int variant, bool exact) {
     case 0: return rows_kernel_for_v<E, 0>(exact);
     case 1: return rows_kernel_for_v<E, 1>(exact);
     case 2: return rows_kernel_for_v<E, 2>(exact);
+    case 4: return rows_kernel_for_v<E, 4>(exact);
     default: return rows_kernel_for_v<E, 3>(exact);
   }
 }
@@ -391,8 +392,8 @@ void* pick_rows(adaln_dtype_t dt, int variant, bool exact) {
 cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
-  return staging_shape(pick_rows(dt, choose_variant(nvec), variant_exact(nvec)), T, D, dt, 2,
-                       kBwdRows, s);
+  const int v = choose_bwd_variant(nvec);
+  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, kBwdRows, v, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,

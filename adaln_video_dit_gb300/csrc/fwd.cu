@@ -243,12 +243,12 @@ void* pick_fwd(adaln_dtype_t dt, int variant, bool exact) {
 // of staged rows per SM, and persistent CTAs = SMs x resident CTAs per SM
 // (at most T).
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
-                          int ntensors, int rows_per_round, Shape* s) {
+                          int ntensors, int rows_per_round, int variant, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   s->row_bytes = D * esize;
   s->nvec = s->row_bytes / 16;
-  s->variant = choose_variant(s->nvec);
-  s->exact = variant_exact(s->nvec);
+  s->variant = variant;
+  s->exact = variant_exact(variant, s->nvec);
   s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
   s->threads = (s->nc + 1) * 32;
@@ -304,8 +304,8 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
-  return staging_shape(pick_fwd(dt, choose_variant(nvec), variant_exact(nvec)), T, D, dt, 1,
-                       kFwdRows, s);
+  const int v = choose_variant(nvec);
+  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, kFwdRows, v, s);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,

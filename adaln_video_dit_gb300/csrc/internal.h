@@ -34,15 +34,22 @@ constexpr int kMaxConsumerWarps = 8;
 //   variant 1: nvec <=  384  VPT 2, <= 6 warps, 2 CTAs/SM
 //   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 CTAs/SM
 //   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 CTA/SM
+//   variant 4: nvec <=  384  VPT 4, <= 3 warps, 3 CTAs/SM (backward only:
+//              its column sums favour few warps per row, many rows per SM)
 ADALN_HD inline int choose_variant(int nvec) {
   return nvec <= 192 ? 0 : (nvec <= 384 ? 1 : (nvec <= 640 ? 2 : 3));
 }
+ADALN_HD inline int choose_bwd_variant(int nvec) {
+  return nvec <= 192 ? 0 : (nvec <= 384 ? 4 : (nvec <= 640 ? 2 : 3));
+}
 ADALN_HD constexpr int variant_vpt(int v) { return v == 0 ? 1 : (v == 1 ? 2 : 4); }
-ADALN_HD constexpr int variant_max_warps(int v) { return v == 2 ? 5 : (v == 3 ? 8 : 6); }
-ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : 2; }
+ADALN_HD constexpr int variant_max_warps(int v) {
+  return v == 2 ? 5 : (v == 3 ? 8 : (v == 4 ? 3 : 6));
+}
+ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : (v == 4 ? 3 : 2); }
 ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
-ADALN_HD inline bool variant_exact(int nvec) {
-  const int v = choose_variant(nvec);
+// The row fills the variant's largest consumer-warp count exactly.
+ADALN_HD inline bool variant_exact(int v, int nvec) {
   return nvec == variant_max_warps(v) * 32 * variant_vpt(v);
 }
 
