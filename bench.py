@@ -46,6 +46,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sites", type=int, default=1,
+                   help="modulation sites per step (mmdit_joint steady state: 60 = 2 per "
+                        "block x 30 blocks), each its own shift/scale, back to back")
+    p.add_argument("--graph", action="store_true",
+                   help="with --sites: replay each step as one captured CUDA graph")
     p.add_argument("--report", choices=["unfused"], default=None,
                    help="instead of the benchmark line: compare with torch's unfused "
                         "chain (time and saved activation bytes)")
@@ -450,6 +455,95 @@ def load_traffic(kernel):
 
 
 # ---------------------------------------------------------------------------
+# Steady state over many modulation sites (the MMDiT joint-stream recipe: the
+# operator runs at 2 sites per block x 30 blocks, each site with its own
+# shift/scale).  A step = every site's forward + backward, back to back, with
+# no L2 eviction between sites; L2 is evicted between steps.
+# ---------------------------------------------------------------------------
+def run_sites(args, rank, local, world, pg):
+    import torch
+    from adaln_video_dit_gb300 import _lib as L
+    from adaln_video_dit_gb300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    c = I.make(WORKLOADS[args.workload], sites=args.sites) if WORKLOADS[args.workload] == 5 \
+        else I.make(WORKLOADS[args.workload])
+    T, D, nseg = c["T"], c["D"], c["nseg"]
+    shifts = c["shift"] if isinstance(c["shift"], list) else [c["shift"]] * args.sites
+    scales = c["scale"] if isinstance(c["scale"], list) else [c["scale"]] * args.sites
+    tdt = torch.bfloat16 if c["dtype"] == "bf16" else torch.float32
+    x, dy, seg = (torch_view(c[k]).to(dev) for k in ("x", "dy", "seg_id"))
+    sh = [torch_view(a).to(dev) for a in shifts]
+    sc = [torch_view(a).to(dev) for a in scales]
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    mean = torch.empty(T, device=dev)
+    rstd = torch.empty(T, device=dev)
+    dsh = torch.empty(args.sites, nseg, D, device=dev)
+    dsc = torch.empty(args.sites, nseg, D, device=dev)
+    ws = torch.empty(L.adaln_bwd_workspace_size(T, D, nseg, tdt), device=dev, dtype=torch.uint8)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, device=dev)
+    flush_out = torch.empty((), device=dev)
+
+    def step(stream):
+        for i in range(args.sites):
+            L.adaln_fwd(x, sh[i], sc[i], seg, c["eps"], y=y, mean=mean, rstd=rstd, stream=stream)
+            L.adaln_bwd(dy, x, mean, rstd, sc[i], seg, dx=dx, dshift=dsh[i], dscale=dsc[i],
+                        workspace=ws, stream=stream)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        step(stream)
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            graph.capture_begin()
+            step(cap)
+            graph.capture_end()
+        stream.wait_stream(cap)
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    rc, bits = L.adaln_get_status()
+    if rc != L.ADALN_OK:
+        raise RuntimeError(f"device status: {L.strerror(rc)} ({bits})")
+    K = args.steps
+    ms = []
+    barrier(pg, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_smi_id(local)) as clocks:
+        for _ in range(K):
+            torch.sum(flush, dim=0, out=flush_out)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step(stream)
+            e1.record(stream)
+            ms.append((e0, e1))
+        torch.cuda.synchronize(dev)
+    barrier(pg, dev)
+    step_ms = max_over_ranks(pg, statistics.mean(a.elapsed_time(b) for a, b in ms), dev)
+    if rank == 0:
+        ab = alg_bytes(T, D, nseg, 2 if tdt == torch.bfloat16 else 4)
+        peak, kind = peaks()
+        gbs = args.sites * ab["fwd_bwd"] / (step_ms * 1e-3) / 1e9
+        out = {"report": "sites_steady_state", "metric": METRIC,
+               "value": world * args.sites * T / (step_ms * 1e-3), "unit": "tokens/s",
+               "n_gpus": world, "steps": K, "ms_per_step": step_ms, "dtype": c["dtype"],
+               "config": {"workload": c["name"], "T": T, "D": D, "nseg": nseg,
+                          "sites": args.sites, "cuda_graph": bool(args.graph),
+                          "launches_per_step": 3 * args.sites},
+               "gbs": gbs, "frac_of_" + kind: gbs / peak, "clocks": clocks.summary()}
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # Context report: torch's unfused chain (layer_norm, gather, multiply, add and
 # their autograd backward) against the fused operator on the same inputs.
 # ---------------------------------------------------------------------------
@@ -558,6 +652,11 @@ def main():
         report_unfused(args)
         return
     rank, local, world, pg = dist_setup(args.gpus)
+    if args.sites > 1 and args.impl == "native":
+        run_sites(args, rank, local, world, pg)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         if pg is not None:
