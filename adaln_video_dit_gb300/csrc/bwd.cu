@@ -368,8 +368,8 @@ namespace {
 
 template <class E, int V>
 void* rows_kernel_for_v(bool exact) {
-  return exact ? reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, kBwdRows, true>)
-               : reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, kBwdRows, false>);
+  return exact ? reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, bwd_rows(V), true>)
+               : reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, bwd_rows(V), false>);
 }
 
 template <class E>
@@ -393,7 +393,7 @@ cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_bwd_variant(nvec);
-  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, kBwdRows, v, s);
+  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,

@@ -218,8 +218,8 @@ namespace {
 
 template <class E, int V>
 void* fwd_kernel_for_v(bool exact) {
-  return exact ? reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, kFwdRows, true>)
-               : reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, kFwdRows, false>);
+  return exact ? reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, fwd_rows(V), true>)
+               : reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, fwd_rows(V), false>);
 }
 
 template <class E>
@@ -305,7 +305,7 @@ cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_variant(nvec);
-  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, kFwdRows, v, s);
+  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, fwd_rows(v), v, s);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,

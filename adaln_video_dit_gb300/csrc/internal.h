@@ -15,11 +15,8 @@
 
 namespace adaln {
 
-// Most rows handled per reduction round (compile-time in the kernels):
-// the forward takes 4 rows per round, the backward 2.
-constexpr int kRowsPerRound = 4;
-constexpr int kFwdRows = 4;
-constexpr int kBwdRows = 2;
+// Most rows handled per reduction round (sizes the reduction scratch).
+constexpr int kRowsPerRound = 8;
 // Largest number of consumer warps in a CTA (any variant).
 constexpr int kMaxConsumerWarps = 8;
 
@@ -48,6 +45,10 @@ ADALN_HD constexpr int variant_max_warps(int v) {
 }
 ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : (v == 4 ? 3 : 2); }
 ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
+// Rows per reduction round.  A round's latency hardly depends on the row
+// length, so short rows take more rows per round (as registers allow).
+ADALN_HD constexpr int fwd_rows(int v) { return v == 0 ? 8 : 4; }
+ADALN_HD constexpr int bwd_rows(int v) { return v == 0 ? 4 : 2; }
 // The row fills the variant's largest consumer-warp count exactly.
 ADALN_HD inline bool variant_exact(int v, int nvec) {
   return nvec == variant_max_warps(v) * 32 * variant_vpt(v);
