@@ -6,11 +6,14 @@
 // the rows, so every warp access is contiguous along d.  Here that column
 // reduction is fused into the row pass: each persistent CTA streams its
 // contiguous row range of x and dy through a shared-memory ring (read from
-// HBM exactly once), computes dx per row, and accumulates dy * xhat and dy in
-// registers of the thread that owns each column.  At a segment change and at
-// the end of its range a CTA writes one fp32 partial per (CTA, segment) to
-// the workspace; a second launch sums the partials of each segment in CTA
-// order.  No floating-point atomics, no inter-CTA waits.
+// HBM exactly once), computes dx per row (phase 1: the two row sums and the
+// column sums; phase 2: dx, both reading the rows from the stage), and
+// accumulates dy * xhat and dy in registers of the thread that owns each
+// column.  At a segment change and at the end of its range a CTA writes one
+// fp32 partial per (CTA, segment) to the workspace, and records the first row
+// of every segment it starts; a second launch (a programmatic dependent)
+// sums the partials of each segment in CTA order.  No floating-point atomics,
+// no inter-CTA waits.
 //
 //   dx[t,d]      = rstd_t (g - mean_d g - xhat mean_d(g xhat)),  g = dy (1 + scale_b)
 //   dscale[b,d]  = sum over rows of segment b of dy xhat

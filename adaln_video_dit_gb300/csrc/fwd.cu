@@ -5,10 +5,11 @@
 // modulation is applied in the same launch, so x is read from HBM once and y
 // written once.  Here each persistent CTA streams its contiguous row range
 // through a shared-memory ring (bulk async copies issued by one producer
-// lane); consumer threads move their column slice of R rows into registers
-// once (widened to fp32), compute the row mean, then the centred sum of
-// squares (two-pass: the exact definition of the biased variance), and write
-// y with 16-byte streaming stores.  Element arithmetic uses packed fp32x2
+// lane); for each round of R rows the consumer threads read their column
+// slice from the stage three times (row sums -> mean; centred sum of squares
+// -> rstd, the two-pass definition of the biased variance; modulate) and
+// write y with 16-byte streaming stores, keeping only the segment's
+// (1 + scale) and shift in registers.  Element arithmetic uses packed fp32x2
 // instructions.
 #include <cstdlib>
 
