@@ -27,7 +27,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ["adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_noalloc",
            "adaln_get_status", "adaln_strerror", "adaln_trace_begin",
            "adaln_trace_end", "adaln_trace_get", "adaln_launch_shape",
-           "adaln_selftest_wait_timeout"]
+           "adaln_selftest_wait_timeout", "adaln_fwd_bwd_host_scratch_size",
+           "adaln_fwd_bwd_host"]
 
 
 class AdalnError(RuntimeError):
@@ -64,6 +65,12 @@ def _load():
     lib.adaln_trace_get.restype = ci
     lib.adaln_trace_get.argtypes = [ci, ctypes.POINTER(ctypes.c_int64),
                                     ctypes.POINTER(ctypes.c_double)]
+    lib.adaln_fwd_bwd_host_scratch_size.restype = ci
+    lib.adaln_fwd_bwd_host_scratch_size.argtypes = [i64, i32, i32, ci, i64,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+    lib.adaln_fwd_bwd_host.restype = ci
+    lib.adaln_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, ci, f32, vp, vp, vp,
+                                       vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
     lib.adaln_selftest_wait_timeout.restype = ci
     lib.adaln_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     lib.adaln_launch_shape.restype = ci
@@ -200,6 +207,57 @@ def adaln_bwd_noalloc(dy, x, mean, rstd, scale, seg_id, dx=None, dshift=None, ds
                                _ptr(dshift), _ptr(dscale), _stream_ptr(stream, x.device))
     _check(rc, "adaln_bwd_noalloc")
     return dx, dshift, dscale
+
+
+def adaln_fwd_bwd_host_scratch_size(T, D, nseg, dtype, chunk_rows=0):
+    """Device scratch bytes adaln_fwd_bwd_host needs."""
+    n = ctypes.c_size_t(0)
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    _check(raw.adaln_fwd_bwd_host_scratch_size(int(T), int(D), int(nseg), code, int(chunk_rows),
+                                               ctypes.byref(n)), "adaln_fwd_bwd_host_scratch_size")
+    return n.value
+
+
+def _host(t, name, dtype=None, shape=None):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def adaln_fwd_bwd_host(x, dy, shift, scale, seg_id, eps, out, scratch, chunk_rows=0,
+                       stream=None):
+    """Forward + backward on host tensors (pinned for overlap), pipelined in row
+    chunks.  `out` is a dict of preallocated host tensors y, mean, rstd, dx,
+    dshift, dscale; `scratch` a uint8 CUDA tensor of at least
+    adaln_fwd_bwd_host_scratch_size bytes.  Asynchronous on `stream`."""
+    T, D = x.shape
+    nseg = shift.shape[0]
+    dt = x.dtype
+    _host(x, "x", dt)
+    _host(dy, "dy", dt, (T, D))
+    _host(shift, "shift", dt, (nseg, D))
+    _host(scale, "scale", dt, (nseg, D))
+    _host(seg_id, "seg_id", torch.int32, (T,))
+    _host(out["y"], "y", dt, (T, D))
+    _host(out["dx"], "dx", dt, (T, D))
+    for k in ("mean", "rstd"):
+        _host(out[k], k, torch.float32, (T,))
+    for k in ("dshift", "dscale"):
+        _host(out[k], k, torch.float32, (nseg, D))
+    _dev(scratch, "scratch")
+    rc = raw.adaln_fwd_bwd_host(_ptr(x), _ptr(dy), _ptr(shift), _ptr(scale), _ptr(seg_id), T, D,
+                                nseg, dtype_code(dt), float(eps), _ptr(out["y"]),
+                                _ptr(out["mean"]), _ptr(out["rstd"]), _ptr(out["dx"]),
+                                _ptr(out["dshift"]), _ptr(out["dscale"]), int(chunk_rows),
+                                _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                _stream_ptr(stream, scratch.device))
+    _check(rc, "adaln_fwd_bwd_host")
 
 
 def adaln_get_status(stream=None, device=None):

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libadaln.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "host.cu", "noalloc.cu", "selftest.cu"]
 HEADERS = ["common.cuh", "ring.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -127,6 +127,68 @@ int cuda_fail(cudaError_t e) {
 
 }  // namespace
 
+namespace adaln {
+
+int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* seg_id,
+            int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, float eps, void* y,
+            float* mean, float* rstd, cudaStream_t st) {
+  if (T == 0) return ADALN_OK;
+  Shape s;
+  cudaError_t e = get_shape(ADALN_KERNEL_FWD, T, D, dtype, &s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned* status = nullptr;
+  e = status_ptr(&status);
+  if (e != cudaSuccess) return cuda_fail(e);
+  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, 1.0f / (float)D, status};
+  e = traced(ADALN_KERNEL_FWD, st, [&] { return launch_fwd(a, dtype, s, st); });
+  return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
+}
+
+int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+            const void* scale, const int32_t* seg_id, int64_t T, int32_t D, int32_t nseg,
+            adaln_dtype_t dtype, void* dx, float* dshift, float* dscale, void* workspace,
+            size_t workspace_bytes, cudaStream_t st, int accumulate) {
+  Shape s;
+  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const size_t need = bwd_workspace_bytes(s, D, nseg);
+  if (workspace_bytes < need) return ADALN_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  e = status_ptr(&status);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  float* partials = static_cast<float*>(workspace);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
+                                                  bwd_partials_bytes(s, D, nseg));
+  BwdArgs a{dy, x, mean, rstd, scale, seg_id, dx, dshift, dscale,
+            partials, seg_start, T, D, nseg, 1.0f / (float)D, status, accumulate};
+  if (T > 0) {
+    e = traced(ADALN_KERNEL_BWD_ROWS, st, [&] { return launch_bwd_rows(a, dtype, s, st); });
+    if (e != cudaSuccess) return cuda_fail(e);
+  } else if (accumulate) {
+    return ADALN_OK;  // nothing to add
+  }
+  e = traced(ADALN_KERNEL_BWD_FINALIZE, st, [&] { return launch_bwd_finalize(a, s, st); });
+  return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
+}
+
+size_t bwd_workspace_need(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, int* rc) {
+  Shape s;
+  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
+  if (e != cudaSuccess) {
+    *rc = cuda_fail(e);
+    return 0;
+  }
+  *rc = ADALN_OK;
+  return (bwd_workspace_bytes(s, D, nseg) + 255) & ~(size_t)255;
+}
+
+int check_dims_public(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dt) {
+  return check_dims(T, D, nseg, dt);
+}
+
+}  // namespace adaln
+
 extern "C" {
 
 int adaln_fwd(const void* x, const void* shift, const void* scale,
@@ -141,17 +203,8 @@ int adaln_fwd(const void* x, const void* shift, const void* scale,
       !aligned(seg_id, 4) || !aligned(mean, 4) || !aligned(rstd, 4))
     return ADALN_ERR_ALIGN;
   if (!std::isfinite(eps) || eps < 0.0f) return ADALN_ERR_ARG;
-
-  Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_FWD, T, D, dtype, &s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  unsigned* status = nullptr;
-  e = status_ptr(&status);
-  if (e != cudaSuccess) return cuda_fail(e);
-  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, 1.0f / (float)D, status};
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = traced(ADALN_KERNEL_FWD, st, [&] { return launch_fwd(a, dtype, s, st); });
-  return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
+  return adaln::run_fwd(x, shift, scale, seg_id, T, D, nseg, dtype, eps, y, mean, rstd,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype,
@@ -182,27 +235,8 @@ int adaln_bwd(const void* dy, const void* x, const float* mean, const float* rst
                 !aligned(seg_id, 4)))
     return ADALN_ERR_ALIGN;
 
-  Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  const size_t need = bwd_workspace_bytes(s, D, nseg);
-  if (workspace_bytes < need) return ADALN_ERR_WORKSPACE;
-  unsigned* status = nullptr;
-  e = status_ptr(&status);
-  if (e != cudaSuccess) return cuda_fail(e);
-
-  float* partials = static_cast<float*>(workspace);
-  int32_t* seg_start = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) +
-                                                  bwd_partials_bytes(s, D, nseg));
-  BwdArgs a{dy, x, mean, rstd, scale, seg_id, dx, dshift, dscale,
-            partials, seg_start, T, D, nseg, 1.0f / (float)D, status};
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (T > 0) {
-    e = traced(ADALN_KERNEL_BWD_ROWS, st, [&] { return launch_bwd_rows(a, dtype, s, st); });
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  e = traced(ADALN_KERNEL_BWD_FINALIZE, st, [&] { return launch_bwd_finalize(a, s, st); });
-  return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
+  return adaln::run_bwd(dy, x, mean, rstd, scale, seg_id, T, D, nseg, dtype, dx, dshift, dscale,
+                        workspace, workspace_bytes, static_cast<cudaStream_t>(stream), 0);
 }
 
 int adaln_get_status(uint32_t* host_bits, void* stream) {

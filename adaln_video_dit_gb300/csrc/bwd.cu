@@ -354,10 +354,15 @@ __global__ void __launch_bounds__(kFinalizeThreads, 4)
     }
   }
   if (g == 0 && col4 < 2 * ncol4) {
-    if (col4 < ncol4)
-      reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D)[col4] = ps;
-    else
-      reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D)[col4 - ncol4] = ps;
+    float4* o = col4 < ncol4
+                    ? reinterpret_cast<float4*>(a.dscale + (size_t)b * a.D) + col4
+                    : reinterpret_cast<float4*>(a.dshift + (size_t)b * a.D) + (col4 - ncol4);
+    if (!a.accumulate) {
+      *o = ps;
+    } else if (eb > sb) {  // a chunk of a row-chunked call: add, in chunk order
+      const float4 u = *o;
+      *o = make_float4(u.x + ps.x, u.y + ps.y, u.z + ps.z, u.w + ps.w);
+    }
   }
 }
 

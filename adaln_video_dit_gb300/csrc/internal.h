@@ -100,6 +100,7 @@ struct BwdArgs {
   int32_t nseg;
   float inv_d;  // 1 / D rounded to fp32
   unsigned* status;
+  int accumulate;  // finalize adds its sums to dshift/dscale (row-chunked calls)
 };
 
 // Launch shapes (depend on the current device).  Return cudaSuccess or the
@@ -126,6 +127,19 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt,
                             const Shape& s, cudaStream_t st);
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s,
                                 cudaStream_t st);
+
+// Launch parts of the C entry points (api.cu), without argument checks; the
+// backward can add its sums into dshift/dscale (accumulate = 1) for callers
+// that process the rows in chunks.
+int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* seg_id,
+            int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, float eps, void* y,
+            float* mean, float* rstd, cudaStream_t st);
+int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+            const void* scale, const int32_t* seg_id, int64_t T, int32_t D, int32_t nseg,
+            adaln_dtype_t dtype, void* dx, float* dshift, float* dscale, void* workspace,
+            size_t workspace_bytes, cudaStream_t st, int accumulate);
+size_t bwd_workspace_need(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, int* rc);
+int check_dims_public(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dt);
 
 // Bounded-wait self-test (selftest.cu).
 cudaError_t launch_wait_timeout_probe(unsigned* status, uint64_t limit_ns, cudaStream_t st);

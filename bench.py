@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--workload", default="long_video", choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-chunk", type=int, default=0,
+                   help="rows per pipelined chunk of the e2e leg (0: the library default)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -298,33 +300,26 @@ def run_native(args, c, rank, local, world, pg):
 
 
 def run_e2e(args, c, h, dev, stream, L, tdt, pg):
-    """Same step through the public API from pinned host buffers: every step
-    copies its inputs host->device, runs fwd + bwd, and copies every result
-    back, all inside the timed region."""
+    """Same step through the public host-buffer entry point
+    (adaln_fwd_bwd_host): every step copies its inputs from pinned host memory
+    to the device, runs fwd + bwd, and copies every result back, all inside
+    the timed region.  The library pipelines the copies and kernels in row
+    chunks over its own streams."""
     import torch
     T, D, nseg = c["T"], c["D"], c["nseg"]
     hin = {k: v.pin_memory() for k, v in h.items()}
-    din = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
     hout = dict(y=torch.empty(T, D, dtype=tdt).pin_memory(),
                 dx=torch.empty(T, D, dtype=tdt).pin_memory(),
                 mean=torch.empty(T, dtype=torch.float32).pin_memory(),
                 rstd=torch.empty(T, dtype=torch.float32).pin_memory(),
                 dshift=torch.empty(nseg, D, dtype=torch.float32).pin_memory(),
                 dscale=torch.empty(nseg, D, dtype=torch.float32).pin_memory())
-    dout = {k: torch.empty_like(v, device=dev) for k, v in hout.items()}
-    ws = torch.empty(max(16, L.adaln_bwd_workspace_size(T, D, nseg, tdt)), device=dev,
-                     dtype=torch.uint8)
+    scratch = torch.empty(L.adaln_fwd_bwd_host_scratch_size(T, D, nseg, tdt, args.e2e_chunk),
+                          device=dev, dtype=torch.uint8)
 
     def step():
-        for k in din:
-            din[k].copy_(hin[k], non_blocking=True)
-        L.adaln_fwd(din["x"], din["shift"], din["scale"], din["seg_id"], c["eps"],
-                    y=dout["y"], mean=dout["mean"], rstd=dout["rstd"], stream=stream)
-        L.adaln_bwd(din["dy"], din["x"], dout["mean"], dout["rstd"], din["scale"],
-                    din["seg_id"], dx=dout["dx"], dshift=dout["dshift"], dscale=dout["dscale"],
-                    workspace=ws, stream=stream)
-        for k in hout:
-            hout[k].copy_(dout[k], non_blocking=True)
+        L.adaln_fwd_bwd_host(hin["x"], hin["dy"], hin["shift"], hin["scale"], hin["seg_id"],
+                             c["eps"], hout, scratch, chunk_rows=args.e2e_chunk, stream=stream)
 
     for _ in range(3):
         step()
@@ -703,7 +698,8 @@ def main():
             "clocks": r["clocks"],
             "e2e": {"value": world * T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                    "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"]},
+                    "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
+                    "api": "adaln_fwd_bwd_host"},
         }
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)

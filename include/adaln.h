@@ -152,6 +152,48 @@ ADALN_API int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean
               void* dx, float* dshift, float* dscale, void* stream);
 
 /*
+ * One forward + backward step on HOST-resident tensors: the operator of
+ * section 2.B of the AdaptiveLoad technical summary, as adaln_fwd followed by
+ * adaln_bwd (the formulas at the top of this file), for training steps whose
+ * tensors live in host memory.  The pages describe no host pipeline; this
+ * entry point is this library's own.
+ *
+ * Rows are processed in chunks of `chunk_rows` (0 = about 32 MB per [rows, D]
+ * tensor and chunk): the copies of chunk i + 1 in and of chunk i - 1 out
+ * overlap the kernels of chunk i, on three internal streams of the current
+ * device.  The step starts after the work already queued on `stream` and
+ * after the previous call of this function on the device; `stream` waits
+ * for the whole step (the host buffers may be read once it has drained).
+ *
+ * Arguments: x, dy, shift, scale, seg_id are HOST pointers read by the step;
+ * y, mean, rstd, dx, dshift, dscale are HOST pointers it writes; shapes and
+ * element types as above.  Page-locked (pinned) host memory lets the copies
+ * run asynchronously; pageable memory works but serialises them.  `scratch`
+ * is DEVICE memory of at least adaln_fwd_bwd_host_scratch_size(T, D, nseg,
+ * dtype, chunk_rows) bytes, 256-byte aligned, owned by the caller; calls on
+ * different scratch buffers may share none of them while in flight.
+ *
+ * Results: y, mean, rstd, dx equal those of the device calls bit for bit;
+ * dshift, dscale add the chunks' per-segment sums in chunk order (a fixed
+ * association, deterministic for a given chunk size).
+ *
+ * Errors: ADALN_ERR_DIM, _DTYPE as for adaln_fwd; ADALN_ERR_NULL for a NULL
+ * pointer (row pointers may be NULL when T = 0); ADALN_ERR_ARG for a bad eps
+ * or a negative chunk_rows; ADALN_ERR_ALIGN when scratch is not 256-byte
+ * aligned; ADALN_ERR_WORKSPACE when
+ * scratch_bytes is too small; ADALN_ERR_CUDA when a copy or launch fails
+ * (work enqueued before the failure may still run).  Device data errors go
+ * to the status word as for the device calls.
+ */
+ADALN_API int adaln_fwd_bwd_host_scratch_size(int64_t T, int32_t D, int32_t nseg,
+              adaln_dtype_t dtype, int64_t chunk_rows, size_t* bytes);
+ADALN_API int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shift,
+              const void* scale, const int32_t* seg_id, int64_t T, int32_t D,
+              int32_t nseg, adaln_dtype_t dtype, float eps, void* y, float* mean,
+              float* rstd, void* dx, float* dshift, float* dscale,
+              int64_t chunk_rows, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word.
  * *host_bits (if non-NULL) receives the ADALN_DEV_* bits.  Returns ADALN_OK,
  * ADALN_ERR_SEG, ADALN_ERR_TIMEOUT or ADALN_ERR_CUDA.  The word is shared by

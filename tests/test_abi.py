@@ -124,3 +124,32 @@ def test_binding_rejects_host_tensors(lib):
         lib.adaln_fwd(x, x[:1], x[:1], torch.zeros(4, dtype=torch.int32), 1e-6)
     with pytest.raises(TypeError):
         lib.dtype_code(torch.float16)
+
+
+def host_step(lib, **kw):
+    a = dict(x=P16, dy=P16, shift=P16, scale=P16, seg=P16, T=10, D=64, nseg=2,
+             dt=lib.ADALN_BF16, eps=1e-6, y=P16b, mean=P16b, rstd=P16b, dx=P16b, dshift=P16b,
+             dscale=P16b, chunk=0, scratch=ctypes.c_void_p(0x100000), sb=1 << 30)
+    a.update(kw)
+    return lib.raw.adaln_fwd_bwd_host(a["x"], a["dy"], a["shift"], a["scale"], a["seg"], a["T"],
+                                      a["D"], a["nseg"], a["dt"], a["eps"], a["y"], a["mean"],
+                                      a["rstd"], a["dx"], a["dshift"], a["dscale"], a["chunk"],
+                                      a["scratch"], a["sb"], None)
+
+
+def test_host_step_argument_checks(lib):
+    assert host_step(lib, dt=2) == lib.ADALN_ERR_DTYPE
+    assert host_step(lib, D=12) == lib.ADALN_ERR_DIM
+    assert host_step(lib, nseg=0) == lib.ADALN_ERR_DIM
+    assert host_step(lib, scratch=None) == lib.ADALN_ERR_NULL
+    assert host_step(lib, dshift=None) == lib.ADALN_ERR_NULL
+    assert host_step(lib, dx=None) == lib.ADALN_ERR_NULL
+    assert host_step(lib, scratch=P_ODD) == lib.ADALN_ERR_ALIGN  # 256-byte rule
+    assert host_step(lib, scratch=ctypes.c_void_p(0x10010)) == lib.ADALN_ERR_ALIGN
+    assert host_step(lib, eps=float("inf")) == lib.ADALN_ERR_ARG
+    assert host_step(lib, chunk=-1) == lib.ADALN_ERR_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.raw.adaln_fwd_bwd_host_scratch_size(10, 64, 2, lib.ADALN_BF16, -5,
+                                                   ctypes.byref(n)) == lib.ADALN_ERR_ARG
+    assert lib.raw.adaln_fwd_bwd_host_scratch_size(10, 64, 2, lib.ADALN_BF16, 0,
+                                                   None) == lib.ADALN_ERR_NULL
