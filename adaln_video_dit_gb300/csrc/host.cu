@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -56,34 +57,37 @@ cudaError_t host_ctx(HostCtx** out) {
 
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Offsets of the device scratch: modulation and gradient sums, the backward
-// workspace of one chunk, then kSlots staging slots of one chunk each.
+// Offsets of the device scratch: modulation rows, gradient sums, seg_id,
+// mean and rstd of all T rows (small: 12 bytes a row, so each crosses the
+// host link in one copy rather than one per chunk), the backward workspace of
+// one chunk, then kSlots staging slots of one chunk of x, dy, y, dx each.
 struct Layout {
-  size_t shift, scale, dshift, dscale, ws, ws_bytes, slot0, slot_bytes;
-  size_t x, dy, y, dx, mean, rstd, seg;  // within a slot
+  size_t shift, scale, dshift, dscale, seg, mean, rstd, ws, ws_bytes, slot0, slot_bytes;
+  size_t x, dy, y, dx;  // within a slot
   size_t total;
 };
 
-Layout layout(int64_t C, int32_t D, int32_t nseg, adaln_dtype_t dt, size_t ws_bytes) {
+Layout layout(int64_t T, int64_t C, int32_t D, int32_t nseg, adaln_dtype_t dt,
+              size_t ws_bytes) {
   const size_t es = dt == ADALN_BF16 ? 2 : 4;
   const size_t mod = up256((size_t)nseg * D * es), grad = up256((size_t)nseg * D * 4);
-  const size_t rowsz = up256((size_t)C * D * es), vec = up256((size_t)C * 4);
+  const size_t vec = up256((size_t)T * 4), rowsz = up256((size_t)C * D * es);
   Layout L;
   L.shift = 0;
   L.scale = mod;
   L.dshift = 2 * mod;
-  L.dscale = 2 * mod + grad;
-  L.ws = 2 * mod + 2 * grad;
+  L.dscale = L.dshift + grad;
+  L.seg = L.dscale + grad;
+  L.mean = L.seg + vec;
+  L.rstd = L.mean + vec;
+  L.ws = L.rstd + vec;
   L.ws_bytes = up256(ws_bytes);
   L.slot0 = L.ws + L.ws_bytes;
   L.x = 0;
   L.dy = rowsz;
   L.y = 2 * rowsz;
   L.dx = 3 * rowsz;
-  L.mean = 4 * rowsz;
-  L.rstd = 4 * rowsz + vec;
-  L.seg = 4 * rowsz + 2 * vec;
-  L.slot_bytes = 4 * rowsz + 3 * vec;
+  L.slot_bytes = 4 * rowsz;
   L.total = L.slot0 + kSlots * L.slot_bytes;
   return L;
 }
@@ -92,6 +96,44 @@ int64_t default_chunk(int32_t D, adaln_dtype_t dt) {
   const int64_t row = (int64_t)D * (dt == ADALN_BF16 ? 2 : 4);
   const int64_t c = ((int64_t)32 << 20) / row;  // about 32 MB per tensor and chunk
   return c < 1 ? 1 : c;
+}
+
+// Row ranges of the chunks.  The first copy in and the last copy out run
+// alone on the host link, so when there are enough rows the pipeline starts
+// and ends with chunks of C/8, C/4 and C/2 rows; the rows between are split
+// into near-equal chunks of at most C rows (no short ragged chunk).
+struct Chunk {
+  int64_t r0, rows;
+};
+
+std::vector<Chunk> chunk_plan(int64_t T, int64_t C) {
+  std::vector<Chunk> v;
+  auto split = [&v](int64_t r0, int64_t n, int64_t C) {
+    const int64_t k = (n + C - 1) / C;
+    for (int64_t i = 0; i < k; ++i) {
+      const int64_t a = r0 + n * i / k, b = r0 + n * (i + 1) / k;
+      v.push_back({a, b - a});
+    }
+  };
+  const int64_t ramp[3] = {C / 8, C / 4, C / 2};
+  const int64_t ramp_rows = 2 * (ramp[0] + ramp[1] + ramp[2]);
+  if (ramp[0] < 1 || T < ramp_rows + C) {
+    split(0, T, C);
+    return v;
+  }
+  int64_t r = 0;
+  for (int i = 0; i < 3; ++i) {
+    v.push_back({r, ramp[i]});
+    r += ramp[i];
+  }
+  const int64_t mid = T - ramp_rows;
+  split(r, mid, C);
+  r += mid;
+  for (int i = 2; i >= 0; --i) {
+    v.push_back({r, ramp[i]});
+    r += ramp[i];
+  }
+  return v;
 }
 
 int fail(cudaError_t) {
@@ -114,7 +156,7 @@ extern "C" int adaln_fwd_bwd_host_scratch_size(int64_t T, int32_t D, int32_t nse
   const int64_t C = chunk_rows ? chunk_rows : default_chunk(D, dtype);
   const size_t ws = bwd_workspace_need(C, D, nseg, dtype, &rc);
   if (rc != ADALN_OK) return rc;
-  *bytes = layout(C, D, nseg, dtype, ws).total;
+  *bytes = layout(T, C, D, nseg, dtype, ws).total;
   return ADALN_OK;
 }
 
@@ -134,7 +176,7 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
   const int64_t C = chunk_rows ? chunk_rows : default_chunk(D, dtype);
   const size_t ws_need = bwd_workspace_need(C, D, nseg, dtype, &rc);
   if (rc != ADALN_OK) return rc;
-  const Layout L = layout(C, D, nseg, dtype, ws_need);
+  const Layout L = layout(T, C, D, nseg, dtype, ws_need);
   if (scratch_bytes < L.total) return ADALN_ERR_WORKSPACE;
 
   std::lock_guard<std::mutex> lk(g_host_mu);
@@ -147,6 +189,9 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
   const size_t mod_bytes = (size_t)nseg * D * es, grad_bytes = (size_t)nseg * D * 4;
   float* d_dshift = reinterpret_cast<float*>(base + L.dshift);
   float* d_dscale = reinterpret_cast<float*>(base + L.dscale);
+  int32_t* d_seg = reinterpret_cast<int32_t*>(base + L.seg);
+  float* d_mean = reinterpret_cast<float*>(base + L.mean);
+  float* d_rstd = reinterpret_cast<float*>(base + L.rstd);
 
 #define ADALN_CK(call)          \
   do {                          \
@@ -165,10 +210,18 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
   ADALN_CK(cudaStreamWaitEvent(cx->d2h, cx->start, 0));
   ADALN_CK(cudaMemcpyAsync(base + L.shift, shift, mod_bytes, cudaMemcpyHostToDevice, cx->h2d));
   ADALN_CK(cudaMemcpyAsync(base + L.scale, scale, mod_bytes, cudaMemcpyHostToDevice, cx->h2d));
+  if (T > 0)
+    ADALN_CK(cudaMemcpyAsync(d_seg, seg_id, (size_t)T * 4, cudaMemcpyHostToDevice, cx->h2d));
   ADALN_CK(cudaEventRecord(cx->mod, cx->h2d));
   ADALN_CK(cudaStreamWaitEvent(cx->comp, cx->mod, 0));
 
-  const int64_t nchunks = (T + C - 1) / C;
+  std::vector<Chunk> plan;
+  try {
+    plan = chunk_plan(T, C);
+  } catch (...) {
+    return ADALN_ERR_CUDA;
+  }
+  const int64_t nchunks = (int64_t)plan.size();
   if (nchunks == 0) {
     ADALN_CK(cudaMemsetAsync(d_dshift, 0, grad_bytes, cx->comp));
     ADALN_CK(cudaMemsetAsync(d_dscale, 0, grad_bytes, cx->comp));
@@ -176,8 +229,7 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
   const size_t row = (size_t)D * es;
   for (int64_t i = 0; i < nchunks; ++i) {
     const int sl = (int)(i % kSlots);
-    const int64_t r0 = i * C;
-    const int64_t rows = T - r0 < C ? T - r0 : C;
+    const int64_t r0 = plan[i].r0, rows = plan[i].rows;
     unsigned char* S = base + L.slot0 + (size_t)sl * L.slot_bytes;
     // Copies in (after the slot's previous chunk has been copied out).
     if (i >= kSlots) ADALN_CK(cudaStreamWaitEvent(cx->h2d, cx->out[sl], 0));
@@ -185,18 +237,15 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
                              rows * row, cudaMemcpyHostToDevice, cx->h2d));
     ADALN_CK(cudaMemcpyAsync(S + L.dy, static_cast<const unsigned char*>(dy) + r0 * row,
                              rows * row, cudaMemcpyHostToDevice, cx->h2d));
-    ADALN_CK(cudaMemcpyAsync(S + L.seg, seg_id + r0, rows * 4, cudaMemcpyHostToDevice, cx->h2d));
     ADALN_CK(cudaEventRecord(cx->in[sl], cx->h2d));
     // Compute: forward, then the backward of the chunk, its sums added in order.
     ADALN_CK(cudaStreamWaitEvent(cx->comp, cx->in[sl], 0));
-    rc = run_fwd(S + L.x, base + L.shift, base + L.scale, reinterpret_cast<int32_t*>(S + L.seg),
-                 rows, D, nseg, dtype, eps, S + L.y, reinterpret_cast<float*>(S + L.mean),
-                 reinterpret_cast<float*>(S + L.rstd), cx->comp);
+    rc = run_fwd(S + L.x, base + L.shift, base + L.scale, d_seg + r0, rows, D, nseg, dtype, eps,
+                 S + L.y, d_mean + r0, d_rstd + r0, cx->comp);
     if (rc != ADALN_OK) return rc;
-    rc = run_bwd(S + L.dy, S + L.x, reinterpret_cast<float*>(S + L.mean),
-                 reinterpret_cast<float*>(S + L.rstd), base + L.scale,
-                 reinterpret_cast<int32_t*>(S + L.seg), rows, D, nseg, dtype, S + L.dx,
-                 d_dshift, d_dscale, base + L.ws, L.ws_bytes, cx->comp, i > 0 ? 1 : 0);
+    rc = run_bwd(S + L.dy, S + L.x, d_mean + r0, d_rstd + r0, base + L.scale, d_seg + r0, rows,
+                 D, nseg, dtype, S + L.dx, d_dshift, d_dscale, base + L.ws, L.ws_bytes,
+                 cx->comp, i > 0 ? 1 : 0);
     if (rc != ADALN_OK) return rc;
     ADALN_CK(cudaEventRecord(cx->done[sl], cx->comp));
     // Copies out.
@@ -205,13 +254,15 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
                              cudaMemcpyDeviceToHost, cx->d2h));
     ADALN_CK(cudaMemcpyAsync(static_cast<unsigned char*>(dx) + r0 * row, S + L.dx, rows * row,
                              cudaMemcpyDeviceToHost, cx->d2h));
-    ADALN_CK(cudaMemcpyAsync(mean + r0, S + L.mean, rows * 4, cudaMemcpyDeviceToHost, cx->d2h));
-    ADALN_CK(cudaMemcpyAsync(rstd + r0, S + L.rstd, rows * 4, cudaMemcpyDeviceToHost, cx->d2h));
     ADALN_CK(cudaEventRecord(cx->out[sl], cx->d2h));
   }
-  // The gradient sums, once every chunk is in.
+  // The statistics and the gradient sums, once every chunk is computed.
   ADALN_CK(cudaEventRecord(cx->done[0], cx->comp));
   ADALN_CK(cudaStreamWaitEvent(cx->d2h, cx->done[0], 0));
+  if (T > 0) {
+    ADALN_CK(cudaMemcpyAsync(mean, d_mean, (size_t)T * 4, cudaMemcpyDeviceToHost, cx->d2h));
+    ADALN_CK(cudaMemcpyAsync(rstd, d_rstd, (size_t)T * 4, cudaMemcpyDeviceToHost, cx->d2h));
+  }
   ADALN_CK(cudaMemcpyAsync(dshift, d_dshift, grad_bytes, cudaMemcpyDeviceToHost, cx->d2h));
   ADALN_CK(cudaMemcpyAsync(dscale, d_dscale, grad_bytes, cudaMemcpyDeviceToHost, cx->d2h));
   ADALN_CK(cudaEventRecord(cx->end, cx->d2h));

@@ -158,12 +158,14 @@ ADALN_API int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean
  * tensors live in host memory.  The pages describe no host pipeline; this
  * entry point is this library's own.
  *
- * Rows are processed in chunks of `chunk_rows` (0 = about 32 MB per [rows, D]
- * tensor and chunk): the copies of chunk i + 1 in and of chunk i - 1 out
- * overlap the kernels of chunk i, on three internal streams of the current
- * device.  The step starts after the work already queued on `stream` and
- * after the previous call of this function on the device; `stream` waits
- * for the whole step (the host buffers may be read once it has drained).
+ * Rows are processed in chunks of at most `chunk_rows` (0 = about 32 MB per
+ * [rows, D] tensor and chunk; shorter chunks at both ends shorten the time
+ * the link carries one direction only): the copies of chunk i + 1 in and of
+ * chunk i - 1 out overlap the kernels of chunk i, on three internal streams
+ * of the current device.  The step starts after the work already queued on
+ * `stream` and after the previous call of this function on the device;
+ * `stream` waits for the whole step (the host buffers may be read once it
+ * has drained).
  *
  * Arguments: x, dy, shift, scale, seg_id are HOST pointers read by the step;
  * y, mean, rstd, dx, dshift, dscale are HOST pointers it writes; shapes and

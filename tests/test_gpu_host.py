@@ -22,7 +22,8 @@ def _host_tensors(c):
 
 CASES = [
     # (T, D, nseg, dtype, lengths, chunk_rows)
-    (5000, 1024, 7, "bf16", None, 1024),     # chunks split segments; ragged last chunk
+    (5000, 1024, 7, "bf16", None, 1024),     # ramped chunk plan; chunks split segments
+    (100, 256, 40, "bf16", None, 8),         # ramp of 1, 2, 4 rows; many short segments
     (300, 1536, 2, "bf16", [120, 180], 1000),  # one chunk, T below the chunk size
     (2049, 512, 3, "f32", [0, 2049, 0], 256),  # fp32, empty first/last segments
     (0, 256, 2, "bf16", [0, 0], 64),           # no rows: gradients are zero
