@@ -370,7 +370,8 @@ __global__ void __launch_bounds__(kFinalizeThreads, 4)
 // Host side.
 // ---------------------------------------------------------------------------
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
-                          int ntensors, int rows_per_round, int variant, Shape* s);
+                          int ntensors, int rows_per_round, int variant, int teams,
+                          int cta_header, Shape* s);
 
 namespace {
 
@@ -401,7 +402,8 @@ cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_bwd_variant(nvec);
-  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v, s);
+  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v, 1,
+                       0, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,

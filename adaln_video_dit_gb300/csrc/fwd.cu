@@ -12,45 +12,76 @@
 // (1 + scale) and shift in registers.  Element arithmetic uses packed fp32x2
 // instructions.
 #include <cstdlib>
+#include <mutex>
 
 #include "ring.cuh"
 
 namespace adaln {
 
+// One CTA per SM holds `teams` teams (consumer warps + a producer warp, each
+// with its own ring); teams claim units of R rows.  With a device-wide
+// counter (a.ticket) all teams share all rows, so SMs that stream faster take
+// more rows (SMs differ by up to a fifth in throughput); without one the
+// CTAs split the rows into contiguous ranges and the teams of a CTA share
+// its range through a shared-memory counter (then a segment's modulation
+// rows are loaded once per team, not once per unit: the mode for many short
+// segments, and for launches captured into CUDA graphs).  Every row's result
+// is independent of which team computes it.
 // EXACT: the row fills the variant's largest consumer-warp count exactly
 // (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
 // the warp count and row length are compile-time constants (offsets fold
 // into immediates, no per-vector guards).
 template <class E, int VARIANT, int R, bool EXACT>
-__global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
-    adaln_fwd_kernel(FwdArgs a, int nc_rt, int stages, int nvec_rt) {
+__global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_threads(VARIANT), 1)
+    adaln_fwd_kernel(FwdArgs a, int nc_rt, int stages, int nvec_rt, int team_bytes) {
   constexpr int VPT = variant_vpt(VARIANT);
   constexpr int NC_X = variant_max_warps(VARIANT);
   const int nc = EXACT ? NC_X : nc_rt;
   const int nvec = EXACT ? NC_X * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;  // float2 pairs per vector
   extern __shared__ __align__(128) unsigned char smem[];
-  const Ring rg = ring_layout(smem, stages);
-  ring_init(rg, nc);
+  const int team_threads = (nc + 1) * 32;
+  const int team = threadIdx.x / team_threads;
+  const int lt = threadIdx.x - team * team_threads;  // thread index in the team
+  int* next_unit = reinterpret_cast<int*>(smem);
+  const Ring rg = ring_layout(smem + kCtaHeaderBytes + team * team_bytes, stages, 1 + team,
+                              team * (nc + 1));
+  if (lt == 0) ring_init_team(rg, nc);
+  if (threadIdx.x == 0) *next_unit = 0;
+  __syncthreads();
 
   const int64_t G = gridDim.x;
   const int64_t r0 = part_begin(blockIdx.x, a.T, G);
   const int64_t nrows = part_begin(blockIdx.x + 1, a.T, G) - r0;
   const int row_bytes = nvec * 16;
-  const int warp = threadIdx.x >> 5;
+  const int warp = lt >> 5;
 
   if (warp == nc) {  // producer warp
-    if ((threadIdx.x & 31) == 0) {
-      const unsigned char* src[1] = {
-          static_cast<const unsigned char*>(a.x) + (size_t)r0 * row_bytes};
-      ring_produce<R, 1>(rg, src, nrows, row_bytes, a.status);
+    if ((lt & 31) == 0) {
+      if (a.ticket != nullptr) {
+        // All rows, units claimed device-wide.  The last producer to finish
+        // (every claim of every producer is done by then) zeroes the
+        // counter pair for the next launch that is given it.
+        const unsigned char* src[1] = {static_cast<const unsigned char*>(a.x)};
+        ring_produce_units<R, 1>(rg, src, 0, a.T, R, row_bytes, a.ticket, a.seg, a.status);
+        __threadfence();
+        const int producers = (int)gridDim.x * (int)(blockDim.x / team_threads);
+        if (atomicAdd(a.ticket + 1, 1) == producers - 1) {
+          a.ticket[0] = 0;
+          __threadfence();
+          a.ticket[1] = 0;
+        }
+      } else {
+        const unsigned char* src[1] = {
+            static_cast<const unsigned char*>(a.x) + (size_t)r0 * row_bytes};
+        ring_produce_units<R, 1>(rg, src, r0, nrows, R, row_bytes, next_unit, a.seg, a.status);
+      }
     }
     return;
   }
 
-  const int j = threadIdx.x;
+  const int j = lt;
   const int NT = nc * 32;
-  const int64_t nchunks = (nrows + R - 1) / R;
   const uint32_t ring0 = smem_addr(rg.ring);
   const uint32_t stage_bytes = (uint32_t)R * row_bytes;
   bool valid[VPT];
@@ -60,52 +91,45 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
   // (1 + scale) and shift of the current segment for this thread's columns.
   float2 s1[VPT][H], sh[VPT][H];
   int cur_b = -1;
-  int prev_b = 0;
-  if (r0 > 0) {
-    int p = a.seg[r0 - 1];
-    prev_b = p < 0 ? 0 : (p >= a.nseg ? a.nseg - 1 : p);
-  }
   int phase = 0;
-
-  // Segment ids are loaded one chunk ahead, so their latency hides behind
-  // the current chunk's work.
-  int n_sg[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) n_sg[r] = r < nrows ? __ldg(a.seg + r0 + r) : 0;
 
   // Every thread's vectors are all in the row when nvec is a multiple of the
   // consumer thread count times VPT (true for D = 1536, 3072, 5120 bf16).
   const bool all_valid = EXACT || nvec == NT * VPT;
 
-  for (int64_t k = 0; k < nchunks; ++k) {
+  for (int64_t k = 0;; ++k) {
     const int s = (int)(k % stages);
     const uint32_t par = (uint32_t)((k / stages) & 1);
-    const int rows = (int)min((int64_t)R, nrows - k * R);
-    const int64_t t0 = r0 + k * R;
+    // The stage's data and meta (unit, segment ids) arrive together.
+    const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
+    const int* m = rg.meta + s * kMetaInts;
+    const int mrows = ok ? m[0] : 0;
+    const bool end = ok && mrows < 0;  // no work left (the same for every warp)
+    const int rows = mrows > 0 ? mrows : 0;
+    const int64_t t0 = rows > 0 ? (int64_t)(uint32_t)m[2] | ((int64_t)m[3] << 32) : 0;
     int sg[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      sg[r] = n_sg[r];
-      const int64_t u = (k + 1) * R + r;
-      n_sg[r] = u < nrows ? __ldg(a.seg + r0 + u) : 0;
-    }
+    for (int r = 0; r < R; ++r) sg[r] = r < rows ? m[4 + r] : 0;
+    int prev_b = 0;
+    if (rows > 0 && m[1] >= 0) prev_b = m[1] >= a.nseg ? a.nseg - 1 : m[1];
 
     // x stays in the stage until the outputs are written: each pass reads
     // its rows from shared memory (registers hold only column state).
-    const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
     const uint32_t st0 = ring0 + s * stage_bytes;
 
-    // One round over the chunk's rows.  FULL (all R rows present, every
-    // vector of this thread in the row, pipeline ok) drops the per-row and
-    // per-vector guards, so the rows' work interleaves freely.
-    auto round = [&](auto full_tag) -> bool {
+    // One round over the unit's rows: 0 = done, 1 = no unit left, 2 = abort.
+    // FULL (all R rows present, every vector of this thread in the row,
+    // pipeline ok) drops the per-row and per-vector guards, so the rows' work
+    // interleaves freely.  The last round (rows = 0) still takes part in the
+    // first team reduction, so that all warps leave the loop together.
+    auto round = [&](auto full_tag) -> int {
       constexpr bool FULL = decltype(full_tag)::value;
       // Pass 1: row sums -> mean.
       float acc[R][1];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float2 t[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        if (FULL || (ok && r < rows)) {
+        if (FULL || r < rows) {
 #pragma unroll
           for (int q = 0; q < VPT; ++q) {
             if (FULL || valid[q]) {
@@ -119,8 +143,9 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
         t[0] = add2(t[0], t[1]);
         acc[r][0] = t[0].x + t[0].y;
       }
-      if (!team_sum<R, 1>(acc, ok, rg, nc, phase)) return false;
+      if (!team_sum<R, 1>(acc, ok, rg, nc, phase)) return 2;
       phase ^= 1;
+      if (end) return 1;
       float mu[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) mu[r] = acc[r][0] * a.inv_d;
@@ -150,7 +175,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
       team_sum<R, 1>(acc, true, rg, nc, phase);
       phase ^= 1;
 
-      // Segment bookkeeping for the chunk's rows, then the modulated outputs.
+      // Segment bookkeeping for the unit's rows, then the modulated outputs.
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         if (FULL || r < rows) {
@@ -197,10 +222,12 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
           }
         }
       }
-      return true;
+      return 0;
     };
     const bool full = ok && rows == R && all_valid;
-    if (!(full ? round(Tag<true>()) : round(Tag<false>()))) {
+    const int rc = full ? round(Tag<true>()) : round(Tag<false>());
+    if (rc == 1) break;
+    if (rc == 2) {
       if (j == 0) {
         atomicOr(a.status, ADALN_DEV_TIMEOUT);
         *rg.abort = 1;
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
       break;
     }
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
+    if ((lt & 31) == 0) mbar_arrive(rg.empty(s));
   }
 }
 
@@ -240,11 +267,14 @@ void* pick_fwd(adaln_dtype_t dt, int variant, bool exact) {
 }  // namespace
 
 // Common shape rule of the staging kernels: the compiled variant for the row
-// length, consumer warps to cover the row, ring depth sized for about 160 KB
-// of staged rows per SM, and persistent CTAs = SMs x resident CTAs per SM
-// (at most T).
+// length, consumer warps to cover the row, `teams` teams per CTA after a
+// `cta_header`-byte CTA header, ring depth
+// sized for about 160 KB of staged rows per SM over the teams the variant is
+// sized for (variant_min_blocks per SM), and persistent CTAs = SMs x resident
+// CTAs per SM (at most T).
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
-                          int ntensors, int rows_per_round, int variant, Shape* s) {
+                          int ntensors, int rows_per_round, int variant, int teams,
+                          int cta_header, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   s->row_bytes = D * esize;
   s->nvec = s->row_bytes / 16;
@@ -252,7 +282,8 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   s->exact = variant_exact(variant, s->nvec);
   s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
-  s->threads = (s->nc + 1) * 32;
+  s->teams = teams;
+  s->threads = teams * (s->nc + 1) * 32;
 
   int dev = 0, sms = 0, optin = 0, smem_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -264,23 +295,29 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   if (e != cudaSuccess) return e;
 
   // Ring depth: about 160 KB of staged rows per SM (ADALN_RING_KB overrides,
-  // for launch-shape sweeps), split over the CTAs the variant is sized for,
+  // for launch-shape sweeps), split over the teams the variant is sized for,
   // and no more than fits beside them.
-  const int ctas = variant_min_blocks(s->variant);
+  const int units = variant_min_blocks(s->variant);  // teams per SM
+  const int ctas = units / teams < 1 ? 1 : units / teams;
   const int stage_bytes = rows_per_round * s->row_bytes * ntensors;
   const int per_cta = smem_sm / ctas - 2048;  // room for the per-CTA reserve
+  const int per_team = (per_cta - cta_header) / teams;
   int ring_kb = 160;
   if (const char* env = getenv("ADALN_RING_KB")) {
     const int v = atoi(env);
     if (v >= 16 && v <= 256) ring_kb = v;
   }
-  int budget = ring_kb * 1024 / ctas;
-  if (budget > per_cta) budget = per_cta;
+  int budget = ring_kb * 1024 / units;
+  if (budget > per_team) budget = per_team;
   int stages = budget / stage_bytes;
   stages = stages < 2 ? 2 : (stages > 16 ? 16 : stages);
-  while (stages > 2 && ring_header_bytes(stages) + stages * stage_bytes > per_cta) --stages;
+  auto team_bytes = [&](int st) {
+    return (ring_header_bytes(st) + st * stage_bytes + 127) & ~127;
+  };
+  while (stages > 2 && team_bytes(stages) > per_team) --stages;
   s->stages = stages;
-  s->smem = ring_header_bytes(stages) + stages * stage_bytes;
+  s->team_bytes = team_bytes(stages);
+  s->smem = cta_header + teams * s->team_bytes;
   if (s->smem > optin) return cudaErrorInvalidValue;
 
   // Allow the device maximum: other D values reuse this template instance
@@ -306,16 +343,114 @@ cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_variant(nvec);
-  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, fwd_rows(v), v, s);
+  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, fwd_rows(v), v,
+                       variant_min_blocks(v), kCtaHeaderBytes, s);
 }
+
+// Device-wide unit counters {next unit, producers done}, one slot per launch
+// in flight.  Zero at module load; the last producer of a launch zeroes its
+// slot again.  A slot is handed to a launch only when the launch that used it
+// before has completed (its event), so no two running launches share one.
+constexpr int kTicketSlots = 256;
+__device__ int g_fwd_tickets[kTicketSlots][2];
+
+namespace {
+
+struct TicketPool {
+  bool ready = false;
+  int* base = nullptr;
+  cudaEvent_t ev[kTicketSlots] = {};
+  bool recorded[kTicketSlots] = {};
+  bool pending[kTicketSlots] = {};  // handed out, event not yet recorded
+  int cursor = 0;
+};
+constexpr int kMaxTicketDevices = 64;
+std::mutex g_ticket_mu;
+TicketPool g_tickets[kMaxTicketDevices];
+
+// A free slot for a launch on `st`, or -1 (then the launch uses CTA-local
+// units).  Launches being captured into a graph get none: a graph may be
+// replayed while other work runs, so it cannot hold a slot.
+int acquire_ticket(cudaStream_t st, int** ptr) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxTicketDevices) return -1;
+  std::lock_guard<std::mutex> lk(g_ticket_mu);
+  TicketPool& p = g_tickets[dev];
+  if (!p.ready) {
+    void* b = nullptr;
+    if (cudaGetSymbolAddress(&b, g_fwd_tickets) != cudaSuccess) return -1;
+    p.base = static_cast<int*>(b);
+    p.ready = true;
+  }
+  for (int i = 0; i < kTicketSlots; ++i) {
+    const int slot = (p.cursor + i) % kTicketSlots;
+    if (p.pending[slot]) continue;
+    if (p.recorded[slot]) {
+      const cudaError_t q = cudaEventQuery(p.ev[slot]);
+      if (q == cudaErrorNotReady) continue;
+      if (q != cudaSuccess) return -1;
+    } else if (p.ev[slot] == nullptr &&
+               cudaEventCreateWithFlags(&p.ev[slot], cudaEventDisableTiming) != cudaSuccess) {
+      return -1;
+    }
+    p.pending[slot] = true;
+    p.cursor = (slot + 1) % kTicketSlots;
+    *ptr = p.base + 2 * slot;
+    return slot;
+  }
+  return -1;
+}
+
+// After the launch: the slot is busy until the work now queued on `st` ends.
+cudaError_t release_ticket(int slot, cudaStream_t st, bool launched) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_ticket_mu);
+  TicketPool& p = g_tickets[dev];
+  p.pending[slot] = false;
+  if (!launched) return cudaSuccess;
+  e = cudaEventRecord(p.ev[slot], st);
+  if (e == cudaSuccess)
+    p.recorded[slot] = true;
+  else
+    p.pending[slot] = true;  // completion unknown: never hand it out again
+  return e;
+}
+
+// Device-wide units pay when a team's consecutive units rarely change
+// segment (a segment's modulation rows are reloaded at each change): when
+// segments are at least 4 rounds of all teams long.  ADALN_FWD_SCHED
+// (= "cta" or "device") forces either mode, for launch-shape sweeps.
+bool want_device_units(const FwdArgs& a, const Shape& s, int R) {
+  if (const char* env = getenv("ADALN_FWD_SCHED")) {
+    if (env[0] == 'c') return false;
+    if (env[0] == 'd') return true;
+  }
+  const int64_t round_rows = (int64_t)s.grid * s.teams * R;
+  return a.T >= 2 * round_rows && a.T / a.nseg >= 4 * round_rows;
+}
+
+}  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st) {
   void* k = pick_fwd(dt, s.variant, s.exact);
-  int nc = s.nc, stages = s.stages, nvec = s.nvec;
+  int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   FwdArgs args = a;
-  void* params[] = {&args, &nc, &stages, &nvec};
-  return cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
+  args.ticket = nullptr;
+  int slot = -1;
+  if (want_device_units(a, s, fwd_rows(s.variant))) slot = acquire_ticket(st, &args.ticket);
+  void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
+  const cudaError_t e = cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
+  if (slot >= 0) {
+    const cudaError_t r = release_ticket(slot, st, e == cudaSuccess);
+    if (e == cudaSuccess && r != cudaSuccess) return r;
+  }
+  return e;
 }
 
 }  // namespace adaln

@@ -17,8 +17,15 @@ namespace adaln {
 
 // Most rows handled per reduction round (sizes the reduction scratch).
 constexpr int kRowsPerRound = 8;
-// Largest number of consumer warps in a CTA (any variant).
+// Largest number of consumer warps in a team (any variant).
 constexpr int kMaxConsumerWarps = 8;
+// Ints of stage meta per ring stage: rows in the stage (-1: no work left),
+// raw segment id of the row before it, first row (low, high 32 bits), then
+// kRowsPerRound segment ids.
+constexpr int kMetaInts = 4 + kRowsPerRound;
+// Bytes before the teams' regions in a staging kernel's shared memory (the
+// unit counter of the teams).
+constexpr int kCtaHeaderBytes = 128;
 
 // Compiled variants of the staging kernels, chosen by the row length in
 // 16-byte vectors (nvec): vectors per thread (VPT), the largest consumer-warp
@@ -58,8 +65,10 @@ struct Shape {
   int variant;    // compiled variant (choose_variant)
   bool exact;     // nvec fills the variant's largest warp count exactly
   int vpt;        // 16-byte vectors per thread per row (1, 2 or 4)
-  int nc;         // consumer warps
-  int threads;    // (nc + 1) * 32: consumers plus one producer warp
+  int nc;         // consumer warps of a team
+  int teams;      // teams per CTA (a team: nc consumer warps + a producer warp)
+  int threads;    // teams * (nc + 1) * 32
+  int team_bytes; // shared memory of one team (header + ring, 128-byte multiple)
   int stages;     // depth of the shared-memory ring
   int smem;       // dynamic shared memory bytes
   int grid;       // persistent CTAs
@@ -81,6 +90,9 @@ struct FwdArgs {
   float eps;
   float inv_d;  // 1 / D rounded to fp32
   unsigned* status;
+  // Device-wide unit counter {next unit, producers done} of this launch, or
+  // nullptr: the teams then share their CTA's contiguous row range only.
+  int* ticket;
 };
 
 struct BwdArgs {
@@ -150,7 +162,8 @@ ADALN_HD inline int ring_header_bytes(int stages) {
   int b = 16 * stages            // full[] and empty[] mbarriers
           + 16                   // abort flag (+ pad)
           + 2 * kMaxConsumerWarps * kRowsPerRound * 2 * 4  // reduction values
-          + 2 * kMaxConsumerWarps * 4;                     // ok flags
+          + 2 * kMaxConsumerWarps * 4                      // ok flags
+          + stages * kMetaInts * 4;                        // stage meta
   return (b + 127) & ~127;
 }
 

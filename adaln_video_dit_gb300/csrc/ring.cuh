@@ -1,6 +1,8 @@
 // Shared-memory staging ring used by the forward and backward row kernels.
 //
-// A CTA = nc consumer warps + 1 producer warp.  The producer (one lane)
+// A team = nc consumer warps + 1 producer warp, with its own ring; a CTA
+// holds one team (backward) or several that share the CTA's rows (forward,
+// ring_produce_units).  The producer (one lane) of a team
 // streams chunks of R consecutive rows from global memory into S ring stages
 // with bulk asynchronous copies, each completing on the stage's "full"
 // mbarrier; consumer warps read the rows from shared memory as often as
@@ -18,42 +20,55 @@
 namespace adaln {
 
 struct Ring {
-  uint32_t base;   // shared address of the dynamic shared memory
+  uint32_t base;   // shared address of this team's header
   int stages;
+  int bar_id;      // named barrier of the team's consumer warps
+  int warp0;       // CTA warp index of the team's first warp
   volatile int* abort;
   float* red;      // [2][kMaxConsumerWarps][R][2]
   int* okf;        // [2][kMaxConsumerWarps]
+  int* meta;       // [stages][kMetaInts]: unit, segment before it, its segments
   unsigned char* ring;
 
   __device__ uint32_t full(int s) const { return base + 8u * s; }
   __device__ uint32_t empty(int s) const { return base + 8u * (stages + s); }
 };
 
-__device__ __forceinline__ Ring ring_layout(unsigned char* smem, int stages) {
+// Layout of one team's region (header, then the 128-byte aligned stages).
+__device__ __forceinline__ Ring ring_layout(unsigned char* smem, int stages, int bar_id = 1,
+                                            int warp0 = 0) {
   Ring r;
   r.base = smem_addr(smem);
   r.stages = stages;
+  r.bar_id = bar_id;
+  r.warp0 = warp0;
   unsigned char* p = smem + 16 * stages;
   r.abort = reinterpret_cast<volatile int*>(p);
   p += 16;
   r.red = reinterpret_cast<float*>(p);
   p += 2 * kMaxConsumerWarps * kRowsPerRound * 2 * 4;
   r.okf = reinterpret_cast<int*>(p);
+  p += 2 * kMaxConsumerWarps * 4;
+  r.meta = reinterpret_cast<int*>(p);
   r.ring = smem + ring_header_bytes(stages);
   return r;
+}
+
+// One thread initialises a team's barriers and abort flag (no CTA sync: the
+// caller follows with __syncthreads before the role split).
+__device__ __forceinline__ void ring_init_team(const Ring& rg, int nc) {
+  for (int s = 0; s < rg.stages; ++s) {
+    mbar_init(rg.full(s), 1);
+    mbar_init(rg.empty(s), nc);
+  }
+  *rg.abort = 0;
+  mbar_init_fence();
 }
 
 // Thread 0 initialises the barriers; everyone syncs.  Must run before the
 // role split (it uses __syncthreads).
 __device__ __forceinline__ void ring_init(const Ring& rg, int nc) {
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < rg.stages; ++s) {
-      mbar_init(rg.full(s), 1);
-      mbar_init(rg.empty(s), nc);
-    }
-    *rg.abort = 0;
-    mbar_init_fence();
-  }
+  if (threadIdx.x == 0) ring_init_team(rg, nc);
   __syncthreads();
 }
 
@@ -99,6 +114,82 @@ __device__ __forceinline__ void ring_produce(const Ring& rg,
   }
 }
 
+// Producer loop of a team that claims its work (one lane).  Rows
+// [r0, r0 + nrows) are cut into units of U rows (a multiple of R) that the
+// teams take in turn from the counter *next_unit (in shared memory: the
+// teams of one CTA share the CTA's range; in global memory: all teams share
+// all rows), so a team that runs faster takes more and all finish together.
+// The next unit is claimed while the current one streams, hiding the
+// counter's latency.  A unit goes through the ring in stages of up to R rows;
+// each stage's meta (rows, raw segment id of the row before it or -1, first
+// row, segment ids of its rows) is written before the producer's arrival on
+// the stage's "full" barrier, which releases it with the data.  When no unit
+// is left the stage gets rows = -1 and no data.  Drains like ring_produce.
+template <int R, int NT>
+__device__ __forceinline__ void ring_produce_units(const Ring& rg,
+                                                   const unsigned char* const (&src)[NT],
+                                                   int64_t r0, int64_t nrows, int U,
+                                                   int row_bytes, int* next_unit,
+                                                   const int32_t* seg, unsigned* status) {
+  const uint64_t policy = l2_evict_first_policy();
+  const int64_t nunits = (nrows + U - 1) / U;
+  const int S = rg.stages;
+  const uint32_t stage_bytes = (uint32_t)R * row_bytes * NT;
+  int64_t issued = 0;
+  int64_t cur = 0, cur_end = 0;  // rows of the current unit not yet staged
+  int next = atomicAdd(next_unit, 1);
+  for (int64_t k = 0;; ++k) {
+    const int s = (int)(k % S);
+    const int64_t it = k / S;
+    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (uint32_t)((it - 1) & 1), rg.abort)) {
+      if (!*rg.abort) atomicOr(status, ADALN_DEV_TIMEOUT);
+      *rg.abort = 1;
+      break;
+    }
+    if (*rg.abort) break;
+    int* m = rg.meta + s * kMetaInts;
+    if (cur == cur_end) {
+      if (next >= nunits) {
+        m[0] = -1;
+        mbar_arrive(rg.full(s));
+        issued = k + 1;
+        break;
+      }
+      cur = (int64_t)next * U;
+      cur_end = min(cur + U, nrows);
+      next = atomicAdd(next_unit, 1);
+    }
+    const int rows = (int)min((int64_t)R, cur_end - cur);
+    const uint32_t bytes = (uint32_t)rows * row_bytes;
+    mbar_expect_tx(rg.full(s), bytes * NT);
+    const uint32_t dst = smem_addr(rg.ring) + (uint32_t)s * stage_bytes;
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+      bulk_g2s(dst + (uint32_t)i * R * row_bytes, src[i] + (size_t)cur * row_bytes, bytes,
+               rg.full(s), policy);
+    // Segment ids load while the copies are in flight.
+    const int64_t t = r0 + cur;
+    int sg[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) sg[r] = r < rows ? __ldg(seg + t + r) : 0;
+    m[1] = t > 0 ? __ldg(seg + t - 1) : -1;
+    m[2] = (int)(t & 0xffffffff);
+    m[3] = (int)(t >> 32);
+#pragma unroll
+    for (int r = 0; r < R; ++r) m[4 + r] = sg[r];
+    m[0] = rows;
+    mbar_arrive(rg.full(s));
+    cur += rows;
+    issued = k + 1;
+  }
+  for (int s = 0; s < S; ++s) {
+    if (issued <= s) break;
+    const int64_t last = s + ((issued - 1 - s) / S) * S;
+    if (!mbar_wait_bounded(rg.full(s), (uint32_t)((last / S) & 1), nullptr))
+      atomicOr(status, ADALN_DEV_TIMEOUT);
+  }
+}
+
 // Sum K values per row over the consumer team, for R rows at once.  Every
 // consumer thread gets bitwise identical sums (butterflies of commutative
 // adds, fixed shape).  `ok` is this thread's pipeline status; the returned
@@ -108,7 +199,7 @@ template <int R, int K>
 __device__ __forceinline__ bool team_sum(float (&v)[R][K], bool ok,
                                          const Ring& rg, int nc, int phase) {
   static_assert(R <= kRowsPerRound && K <= 2, "reduction buffer too small");
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - rg.warp0;
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -128,7 +219,7 @@ __device__ __forceinline__ bool team_sum(float (&v)[R][K], bool ok,
       for (int q = 0; q < K; ++q) red[(w * kRowsPerRound + r) * 2 + q] = v[r][q];
     okf[w] = warp_ok ? 1 : 0;
   }
-  named_barrier_sync(1, nc * 32);
+  named_barrier_sync(rg.bar_id, nc * 32);
   // nc <= 8: every group of 8 lanes reduces the nc warp sums (the same
   // values in the same order), so all lanes end with identical bits.
   const int src = lane & 7;
@@ -147,7 +238,8 @@ __device__ __forceinline__ bool team_sum(float (&v)[R][K], bool ok,
 }
 
 // Read a row's segment id, clamp it into [0, nseg) and record range / order
-// violations (thread 0 of the CTA only reports).
+// violations (lane 0 of each warp reports; errors only, so the extra atomics
+// cost nothing on valid input).
 __device__ __forceinline__ int checked_seg(int raw, int prev, int nseg,
                                            unsigned* status) {
   int b = raw;
@@ -157,7 +249,7 @@ __device__ __forceinline__ int checked_seg(int raw, int prev, int nseg,
     b = b < 0 ? 0 : nseg - 1;
   }
   if (b < prev) bad |= ADALN_DEV_SEG_ORDER;
-  if (bad && threadIdx.x == 0) atomicOr(status, bad);
+  if (bad && (threadIdx.x & 31) == 0) atomicOr(status, bad);
   return b;
 }
 
