@@ -64,6 +64,17 @@ cudaError_t get_shape(int which, int64_t T, int32_t D, adaln_dtype_t dt, Shape* 
   }
   *out = full;
   out->grid = (int)(T < full.grid ? (T < 1 ? 1 : T) : full.grid);
+  if (which == ADALN_KERNEL_BWD_ROWS && T < virtual_ctas(full)) {
+    // Every team of the backward owns a row range of its own: at most T of
+    // them (fewer CTAs, or one team per CTA when T < teams).
+    if (T >= full.teams) {
+      out->grid = (int)(T / full.teams);
+    } else {
+      out->teams = 1;
+      out->threads = (full.nc + 1) * 32;
+      out->smem = full.team_bytes;
+    }
+  }
   return cudaSuccess;
 }
 

@@ -75,9 +75,15 @@ __device__ __forceinline__ void flush_partials(float* partials, int64_t slot, in
 // (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
 // the warp count and row length are compile-time constants (offsets fold
 // into immediates, no per-vector guards).
+//
+// A CTA holds `teams` teams (one per SM share of the variant); team k of CTA c
+// owns the contiguous row range of virtual CTA v = c * teams + k, so the
+// ranges, partial slots and sums are those of teams x grid independent CTAs,
+// while the teams of one SM, being one CTA, get equal shares of it (two
+// separate CTAs on an SM run up to a tenth apart).
 template <class E, int VARIANT, int R, bool EXACT>
-__global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_blocks(VARIANT))
-    adaln_bwd_rows_kernel(BwdArgs a, int nc_rt, int stages, int nvec_rt) {
+__global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_threads(VARIANT), 1)
+    adaln_bwd_rows_kernel(BwdArgs a, int nc_rt, int stages, int nvec_rt, int team_bytes) {
   constexpr int VPT = variant_vpt(VARIANT);
   constexpr int NC_X = variant_max_warps(VARIANT);
   const int nc = EXACT ? NC_X : nc_rt;
@@ -87,17 +93,23 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
   // Let the finalize grid be scheduled as soon as SMs free up; it waits for
   // this grid's completion before reading anything.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const Ring rg = ring_layout(smem, stages);
-  ring_init(rg, nc);
+  const int team_threads = (nc + 1) * 32;
+  const int teams = blockDim.x / team_threads;
+  const int team = threadIdx.x / team_threads;
+  const int lt = threadIdx.x - team * team_threads;  // thread index in the team
+  const Ring rg = ring_layout(smem + team * team_bytes, stages, 1 + team, team * (nc + 1));
+  if (lt == 0) ring_init_team(rg, nc);
+  __syncthreads();
 
-  const int64_t G = gridDim.x;
-  const int64_t r0 = part_begin(blockIdx.x, a.T, G);
-  const int64_t nrows = part_begin(blockIdx.x + 1, a.T, G) - r0;
+  const int64_t G = (int64_t)gridDim.x * teams;  // virtual CTAs
+  const int64_t v = (int64_t)blockIdx.x * teams + team;
+  const int64_t r0 = part_begin(v, a.T, G);
+  const int64_t nrows = part_begin(v + 1, a.T, G) - r0;
   const int row_bytes = nvec * 16;
-  const int warp = threadIdx.x >> 5;
+  const int warp = lt >> 5;
 
   if (warp == nc) {  // producer warp: R rows of x, then R rows of dy, per stage
-    if ((threadIdx.x & 31) == 0) {
+    if ((lt & 31) == 0) {
       const unsigned char* src[2] = {
           static_cast<const unsigned char*>(a.x) + (size_t)r0 * row_bytes,
           static_cast<const unsigned char*>(a.dy) + (size_t)r0 * row_bytes};
@@ -106,7 +118,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
     return;
   }
 
-  const int j = threadIdx.x;
+  const int j = lt;
   const int NT = nc * 32;
   const int64_t nchunks = (nrows + R - 1) / R;
   const uint32_t ring0 = smem_addr(rg.ring);
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
         break;
       }
       __syncwarp();
-      if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty(s));
+      if ((lt & 31) == 0) mbar_arrive(rg.empty(s));
 #pragma unroll
       for (int r = 0; r < R; ++r)
         if (r == rows - 1) prev_last = cb[r];
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(variant_max_threads(VARIANT), variant_min_bloc
       if (k < nchunks) advance(k);
     }
     if (!aborted)
-      flush_partials<E, VPT>(a.partials, blockIdx.x + run_seg, a.D, j, NT, valid, acc_s, acc_b);
+      flush_partials<E, VPT>(a.partials, v + run_seg, a.D, j, NT, valid, acc_s, acc_b);
   }
   // The CTA owning the last row closes the table: segments after the last
   // one present start (and end) at T.
@@ -402,26 +414,26 @@ cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_bwd_variant(nvec);
-  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v, 1,
-                       0, s);
+  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v,
+                       variant_min_blocks(v), 0, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
                             cudaStream_t st) {
   void* k = pick_rows(dt, s.variant, s.exact);
-  int nc = s.nc, stages = s.stages, nvec = s.nvec;
+  int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   BwdArgs args = a;
-  void* params[] = {&args, &nc, &stages, &nvec};
+  void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
   return cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
 }
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {
   // Slot groups per column: about 4-8 partials per group for the longest
   // segments (power of two, 1..64), a single group when segments are short.
-  const int64_t per_seg = ((int64_t)s.grid + a.nseg - 1) / a.nseg;
+  const int64_t per_seg = (virtual_ctas(s) + a.nseg - 1) / a.nseg;
   int gpc = 1;
   while (gpc < 64 && per_seg > 8 * gpc) gpc *= 2;
-  int G = s.grid;
+  int G = (int)virtual_ctas(s);
   BwdArgs args = a;
   void* params[] = {&args, &G, &gpc};
   cudaLaunchConfig_t cfg = {};

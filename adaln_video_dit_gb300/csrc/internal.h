@@ -121,8 +121,11 @@ cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s);
 cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s);
 
 // Number of fp32 partial slots of the backward: G + nseg - 1.
+// Row ranges of the staging kernels are owned by teams: team k of CTA c is
+// virtual CTA c * teams + k of grid * teams.
+inline int64_t virtual_ctas(const Shape& s) { return (int64_t)s.grid * s.teams; }
 inline int64_t bwd_slots(const Shape& s, int32_t nseg) {
-  return (int64_t)s.grid + nseg - 1;
+  return virtual_ctas(s) + nseg - 1;
 }
 
 // Backward workspace: the partial slots, then the segment start table.

@@ -58,6 +58,7 @@ def test_mmdit_joint_sites(adaln):
 EDGE = [
     # (T, D, nseg, dtype, lengths); nvec = 16-byte vectors per row
     (1, 64, 1, "bf16", None),
+    (3, 5120, 2, "bf16", [1, 2]),   # fewer rows than backward teams on the GPU
     (1, 4, 1, "f32", None),
     (7, 8, 3, "bf16", [0, 7, 0]),          # T below the grid; empty first/last segment
     (1001, 136, 5, "bf16", None),          # ragged: odd T, nvec = 17
@@ -228,9 +229,15 @@ def test_trace_counts_launches(adaln):
 
 def test_launch_shape_matches_the_rules(adaln):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # D = 5120 bf16: 640 vectors, 4 per thread -> 5 consumer warps + 1 producer.
+    # D = 5120 bf16: 640 vectors, 4 per thread -> teams of 5 consumer warps +
+    # 1 producer, two teams per CTA, one CTA per SM.
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 32760, 5120, 1, torch.bfloat16)
-    assert s["threads"] == 6 * 32 and s["grid"] % sms == 0 and s["stages"] >= 2
+    assert s["threads"] == 2 * 6 * 32 and s["grid"] == sms and s["stages"] >= 2
+    # Every backward team owns rows: fewer CTAs, then one team, for tiny T.
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 7, 5120, 1, torch.bfloat16)
+    assert s["grid"] == 3 and s["threads"] == 2 * 6 * 32
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 1, 5120, 1, torch.bfloat16)
+    assert s["grid"] == 1 and s["threads"] == 6 * 32
     # D = 1536 bf16: 192 vectors, 1 per thread -> 6 consumer warps; the
     # forward runs one CTA per SM with two teams of 6 + 1 warps.
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 8192, 1536, 2, torch.bfloat16)
