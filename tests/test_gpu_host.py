@@ -62,3 +62,49 @@ def test_host_pipeline_matches_device_path(adaln, T, D, nseg, dtype, lengths, ch
                                            want_dx=False)
     H.check_norm("dshift", dtype, H.to_f64(out["dshift"]), dsh_ref)
     H.check_norm("dscale", dtype, H.to_f64(out["dscale"]), dsc_ref)
+
+
+def test_host_pipeline_from_two_threads(adaln):
+    """Two host threads run the pipelined step at once, each with its own
+    buffers and scratch: the calls are serialised on the device's internal
+    streams and both give the device path's results."""
+    import threading
+    cases = [I.random_case(900 + i, 3000 + 500 * i, 2048, 3, dtype="bf16", dy_std=1.0)
+             for i in range(2)]
+    refs, jobs = [], []
+    for c in cases:
+        T, D, nseg = c["T"], c["D"], c["nseg"]
+        refs.append(H.run_gpu(H.device_inputs(c), c["eps"]))
+        h = _host_tensors(c)
+        out = dict(y=torch.empty(T, D, dtype=torch.bfloat16).pin_memory(),
+                   dx=torch.empty(T, D, dtype=torch.bfloat16).pin_memory(),
+                   mean=torch.empty(T).pin_memory(), rstd=torch.empty(T).pin_memory(),
+                   dshift=torch.empty(nseg, D).pin_memory(),
+                   dscale=torch.empty(nseg, D).pin_memory())
+        scratch = torch.empty(adaln.adaln_fwd_bwd_host_scratch_size(T, D, nseg, torch.bfloat16, 512),
+                              device="cuda", dtype=torch.uint8)
+        jobs.append((c, h, out, scratch))
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(c, h, out, scratch):
+        try:
+            s = torch.cuda.Stream()
+            for _ in range(5):
+                adaln.adaln_fwd_bwd_host(h["x"], h["dy"], h["shift"], h["scale"], h["seg_id"],
+                                         c["eps"], out, scratch, chunk_rows=512, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=j) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (c, h, out, scratch), ref in zip(jobs, refs):
+        for k in ("y", "dx", "mean", "rstd"):
+            assert torch.equal(out[k], ref[k].cpu()), k
+        assert H.normwise(H.to_f64(out["dshift"]), H.to_f64(ref["dshift"])) < 1e-5
+    H.status_ok()

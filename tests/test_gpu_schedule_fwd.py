@@ -90,3 +90,29 @@ def test_concurrent_streams(adaln, sched):
     for o, r in zip(outs, refs):
         assert torch.equal(o["y"], r[0]) and torch.equal(o["mean"], r[1])
     H.status_ok()
+
+
+def test_graph_capture_uses_cta_local_units(adaln, sched):
+    """A long-segment forward (device-wide units when launched eagerly) captured
+    into a CUDA graph runs with CTA-local units and gives the same bits."""
+    sched(None)
+    c = I.random_case(77, 24000, 5120, 1, dtype="bf16")
+    d = H.device_inputs(c)
+    ref = [t.clone() for t in _fwd(adaln, d, c["eps"])]
+    out = {k: torch.empty_like(v) for k, v in zip(("y", "mean", "rstd"), ref)}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _fwd(adaln, d, c["eps"], stream=s, out=out)
+        g = torch.cuda.CUDAGraph()
+        g.capture_begin()
+        _fwd(adaln, d, c["eps"], stream=s, out=out)
+        g.capture_end()
+    torch.cuda.current_stream().wait_stream(s)
+    for k in out:
+        out[k].zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out["y"], ref[0]) and torch.equal(out["rstd"], ref[2])
+    H.status_ok()
