@@ -75,16 +75,41 @@ def build(force=False, verbose=False, ptxas_info=False):
 
 
 
+def _strip_comments(text):
+    """C/C++ source without comments and blank-space differences (string and
+    character literals kept), so that edits to comments keep the hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
-    """sha256 over the CUDA sources and headers (identifies a kernel build)."""
+    """sha256 over the CUDA sources and headers with comments removed
+    (identifies a kernel build's code)."""
     import hashlib
     h = hashlib.sha256()
     for f in sorted(_deps()):
         if f.endswith(".py"):
             continue
-        with open(f, "rb") as fh:
+        with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,

@@ -4,24 +4,25 @@
 // coalesced reduction"): the modulation gradients are reduced along the
 // sequence by threads that each own a feature column d and accumulate down
 // the rows, so every warp access is contiguous along d.  Here that column
-// reduction is fused into the row pass: each persistent CTA streams its
-// contiguous row range of x and dy through a shared-memory ring (read from
-// HBM exactly once), computes dx per row (phase 1: the two row sums and the
-// column sums; phase 2: dx, both reading the rows from the stage), and
+// reduction is fused into the row pass: each persistent team (consumer warps
+// + a producer warp; a CTA per SM holds two or three) streams the contiguous
+// row range of its virtual CTA through a shared-memory ring (x and dy read
+// from HBM exactly once), computes dx per row (phase 1: the two row sums and
+// the column sums; phase 2: dx, both reading the rows from the stage), and
 // accumulates dy * xhat and dy in registers of the thread that owns each
-// column.  At a segment change and at the end of its range a CTA writes one
-// fp32 partial per (CTA, segment) to the workspace, and records the first row
-// of every segment it starts; a second launch (a programmatic dependent)
-// sums the partials of each segment in CTA order.  No floating-point atomics,
-// no inter-CTA waits.
+// column.  At a segment change and at the end of its range a team writes one
+// fp32 partial per (virtual CTA, segment) to the workspace, and records the
+// first row of every segment it starts; a second launch (a programmatic
+// dependent) sums the partials of each segment in virtual-CTA order.  No
+// floating-point atomics, no inter-CTA waits.
 //
 //   dx[t,d]      = rstd_t (g - mean_d g - xhat mean_d(g xhat)),  g = dy (1 + scale_b)
 //   dscale[b,d]  = sum over rows of segment b of dy xhat
 //   dshift[b,d]  = sum over rows of segment b of dy
 //
-// Partial slots: the (CTA c, segment b) pairs met along the rows form a
-// monotone path in which every step increases c, b or both, so slot c + b is
-// unique per pair and G + nseg - 1 slots suffice.
+// Partial slots: the (virtual CTA v, segment b) pairs met along the rows form
+// a monotone path in which every step increases v, b or both, so slot v + b
+// is unique per pair and G + nseg - 1 slots suffice (G virtual CTAs).
 #include "ring.cuh"
 
 namespace adaln {

@@ -3,8 +3,9 @@
 // AdaptiveLoad, Technical summary section 2.B, forward pass: statistics are
 // reduced on chip in two stages (warp shuffles, then across warps) and the
 // modulation is applied in the same launch, so x is read from HBM once and y
-// written once.  Here each persistent CTA streams its contiguous row range
-// through a shared-memory ring (bulk async copies issued by one producer
+// written once.  Here persistent teams (consumer warps + a producer warp,
+// two or three per CTA, one CTA per SM) claim units of R rows and stream them
+// through their shared-memory rings (bulk async copies issued by one producer
 // lane); for each round of R rows the consumer threads read their column
 // slice from the stage three times (row sums -> mean; centred sum of squares
 // -> rstd, the two-pass definition of the biased variance; modulate) and
