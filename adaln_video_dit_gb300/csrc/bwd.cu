@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   advance(0);
 
   int64_t k = 0;  // current chunk
+  int ks = 0;     // its ring stage, k % stages (kept by increment: no 64-bit division)
+  uint32_t kpar = 0;  // parity of its use of that stage, (k / stages) & 1
   int lo = 0;     // first row of chunk k not yet processed
   bool ok = true;
   while (k < nchunks && !aborted) {
@@ -206,8 +208,8 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
         if (r == hi && r < rows && cb[r] == run_seg) hi = r + 1;
       if (hi == lo) break;  // row lo starts the next run
 
-      const int s = (int)(k % stages);
-      if (lo == 0) ok = mbar_wait_bounded(rg.full(s), (uint32_t)((k / stages) & 1), rg.abort);
+      const int s = ks;
+      if (lo == 0) ok = mbar_wait_bounded(rg.full(s), kpar, rg.abort);
       const uint32_t st0 = ring0 + s * stage_bytes;
 
       // Phase 1: xhat, g; column sums; the two row partials.
@@ -287,6 +289,10 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
       for (int r = 0; r < R; ++r)
         if (r == rows - 1) prev_last = cb[r];
       ++k;
+      if (++ks == stages) {
+        ks = 0;
+        kpar ^= 1;
+      }
       lo = 0;
       if (k < nchunks) advance(k);
     }

@@ -98,9 +98,9 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   // consumer thread count times VPT (true for D = 1536, 3072, 5120 bf16).
   const bool all_valid = EXACT || nvec == NT * VPT;
 
-  for (int64_t k = 0;; ++k) {
-    const int s = (int)(k % stages);
-    const uint32_t par = (uint32_t)((k / stages) & 1);
+  int s = 0;          // ring stage of this round (advanced by increment)
+  uint32_t par = 0;   // parity of this use of the stage
+  for (;; s = (s + 1 == stages ? 0 : s + 1), par ^= (s == 0 ? 1u : 0u)) {
     // The stage's data and meta (unit, segment ids) arrive together.
     const bool ok = mbar_wait_bounded(rg.full(s), par, rg.abort);
     const int* m = rg.meta + s * kMetaInts;

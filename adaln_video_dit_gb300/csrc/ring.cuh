@@ -86,10 +86,10 @@ __device__ __forceinline__ void ring_produce(const Ring& rg,
   const int S = rg.stages;
   const uint32_t stage_bytes = (uint32_t)R * row_bytes * NT;
   int64_t issued = 0;
-  for (int64_t k = 0; k < nchunks; ++k) {
-    const int s = (int)(k % S);
-    const int64_t it = k / S;
-    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (uint32_t)((it - 1) & 1), rg.abort)) {
+  int s = 0;        // stage of chunk k (k % S, advanced by increment)
+  uint32_t it = 0;  // use of that stage (k / S), for the "empty" parity
+  for (int64_t k = 0; k < nchunks; ++k, it += (s + 1 == S), s = (s + 1 == S ? 0 : s + 1)) {
+    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (it - 1) & 1, rg.abort)) {
       if (!*rg.abort) atomicOr(status, ADALN_DEV_TIMEOUT);
       *rg.abort = 1;
       break;
@@ -138,10 +138,10 @@ __device__ __forceinline__ void ring_produce_units(const Ring& rg,
   int64_t issued = 0;
   int64_t cur = 0, cur_end = 0;  // rows of the current unit not yet staged
   int next = atomicAdd(next_unit, 1);
-  for (int64_t k = 0;; ++k) {
-    const int s = (int)(k % S);
-    const int64_t it = k / S;
-    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (uint32_t)((it - 1) & 1), rg.abort)) {
+  int s = 0;        // stage of claim k (k % S, advanced by increment)
+  uint32_t it = 0;  // use of that stage (k / S), for the "empty" parity
+  for (int64_t k = 0;; ++k, it += (s + 1 == S), s = (s + 1 == S ? 0 : s + 1)) {
+    if (it > 0 && !mbar_wait_bounded(rg.empty(s), (it - 1) & 1, rg.abort)) {
       if (!*rg.abort) atomicOr(status, ADALN_DEV_TIMEOUT);
       *rg.abort = 1;
       break;
