@@ -83,7 +83,7 @@ typedef enum {
   ADALN_ERR_ALIGN = 3,     /* a pointer is not aligned as required */
   ADALN_ERR_DTYPE = 4,     /* unknown dtype */
   ADALN_ERR_SEG = 5,       /* device status: seg_id out of range or decreasing */
-  ADALN_ERR_WORKSPACE = 6, /* workspace NULL or smaller than required */
+  ADALN_ERR_WORKSPACE = 6, /* workspace smaller than required */
   ADALN_ERR_CUDA = 7,      /* a CUDA runtime call or launch failed */
   ADALN_ERR_ARG = 8,       /* eps negative or not finite; bad trace argument */
   ADALN_ERR_TIMEOUT = 9    /* device status: an internal pipeline wait gave up */
@@ -121,6 +121,8 @@ ADALN_API int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg,
  * bitwise reproducible.  `workspace` (>= adaln_bwd_workspace_size bytes,
  * 16-byte aligned) is scratch owned by the caller; its contents on entry do
  * not matter.  Calls sharing one workspace must not overlap on the device.
+ * A NULL workspace is ADALN_ERR_NULL (adaln_bwd_noalloc serves callers
+ * without one); a short one is ADALN_ERR_WORKSPACE.
  */
 ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
               const float* rstd, const void* scale, const int32_t* seg_id,
