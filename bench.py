@@ -53,9 +53,10 @@ def parse_args():
                         "block x 30 blocks), each its own shift/scale, back to back")
     p.add_argument("--graph", action="store_true",
                    help="with --sites: replay each step as one captured CUDA graph")
-    p.add_argument("--report", choices=["unfused"], default=None,
+    p.add_argument("--report", choices=["unfused", "shapes"], default=None,
                    help="instead of the benchmark line: compare with torch's unfused "
-                        "chain (time and saved activation bytes)")
+                        "chain (time and saved activation bytes), or shape-benchmark "
+                        "the operator and fit the step-time cost model")
     return p.parse_args()
 
 
@@ -551,6 +552,33 @@ def run_sites(args, rank, local, world, pg):
 # Context report: torch's unfused chain (layer_norm, gather, multiply, add and
 # their autograd backward) against the fused operator on the same inputs.
 # ---------------------------------------------------------------------------
+def report_shapes(args):
+    """Shape benchmarking (AdaptiveLoad, Technical summary section 2.A) of the
+    fused operator itself: fwd + bwd time over a grid of (B samples, S tokens)
+    at D = 5120 bf16, the fit t ~ a + b*B*S**p, and the compute bound M_comp
+    and bucket sizes B_shape(S) it implies for a target step time."""
+    import torch
+    from adaln_video_dit_gb300 import schedule as Sch
+
+    torch.cuda.set_device(0)
+    shapes = [(B, S) for S in (1024, 4096, 16384, 32760) for B in (1, 2, 4, 8)]
+    res = Sch.shape_benchmark(shapes, D=5120, steps=20, warmup=3)
+    Bs, Ss, ts = zip(*res)
+    a, b, p = Sch.fit_cost_model(Bs, Ss, ts)
+    tau = 1.0  # ms
+    m_comp = Sch.m_comp_for_step_time(a, b, tau)
+    buckets = Sch.bucket_plan([256, 1024, 4096, 16384, 32760], 65536, m_comp, p)
+    rel = [abs(float(Sch.cost_model(B_, S_, a, b, p)) - t_) / t_ for B_, S_, t_ in res]
+    print(json.dumps({
+        "report": "shape_benchmark", "device": torch.cuda.get_device_name(0),
+        "D": 5120, "dtype": "bf16", "step": "adaln_fwd + adaln_bwd, one segment per sample",
+        "points_B_S_ms": [[int(B_), int(S_), round(t_, 5)] for B_, S_, t_ in res],
+        "fit": {"a_ms": a, "b_ms_per_token_p": b, "p": p,
+                "max_rel_residual": max(rel)},
+        "target_step_ms": tau, "m_comp": m_comp, "m_mem": 65536,
+        "b_shape": {str(k): v for k, v in buckets.items()}}))
+
+
 def report_unfused(args):
     import torch
     import torch.nn.functional as F
@@ -654,6 +682,9 @@ def main():
     args = parse_args()
     if args.report == "unfused":
         report_unfused(args)
+        return
+    if args.report == "shapes":
+        report_shapes(args)
         return
     rank, local, world, pg = dist_setup(args.gpus)
     if args.sites > 1 and args.impl == "native":
