@@ -14,6 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libadaln.so")
+LIB_TUNING = os.path.join(HERE, "libadaln_tuning.so")
 SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "host.cu", "noalloc.cu", "selftest.cu"]
 HEADERS = ["common.cuh", "ring.cuh", "internal.h"]
 
@@ -37,22 +38,31 @@ def _deps():
     return files
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force=False, verbose=False, ptxas_info=False):
-    """Compile libadaln.so if missing or stale; return its path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force=False, verbose=False, ptxas_info=False, tuning=False):
+    """Compile libadaln.so if missing or stale; return its path.
+
+    tuning=True builds libadaln_tuning.so instead, with -DADALN_TUNING: that
+    copy reads the launch-shape sweep variables ADALN_RING_KB,
+    ADALN_CTAS_PER_SM and ADALN_FWD_SCHED.  The release library (and the
+    binding, which loads only libadaln.so) reads no environment variable."""
+    lib = LIB_TUNING if tuning else LIB
+    if not force and not _stale(lib):
+        return lib
+    out_dir = OUT_DIR + ("_tuning" if tuning else "")
+    os.makedirs(out_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if tuning:
+        extra.append("-DADALN_TUNING")
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,13 +75,13 @@ def build(force=False, verbose=False, ptxas_info=False):
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 
@@ -113,4 +123,4 @@ def source_hash():
     return h.hexdigest()[:16]
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                ptxas_info="--ptxas" in sys.argv))
+                ptxas_info="--ptxas" in sys.argv, tuning="--tuning" in sys.argv))

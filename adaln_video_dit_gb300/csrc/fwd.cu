@@ -295,19 +295,22 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
     e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
 
-  // Ring depth: about 160 KB of staged rows per SM (ADALN_RING_KB overrides,
-  // for launch-shape sweeps), split over the teams the variant is sized for,
-  // and no more than fits beside them.
+  // Ring depth: about 160 KB of staged rows per SM, split over the teams the
+  // variant is sized for, and no more than fits beside them.
   const int units = variant_min_blocks(s->variant);  // teams per SM
   const int ctas = units / teams < 1 ? 1 : units / teams;
   const int stage_bytes = rows_per_round * s->row_bytes * ntensors;
   const int per_cta = smem_sm / ctas - 2048;  // room for the per-CTA reserve
   const int per_team = (per_cta - cta_header) / teams;
   int ring_kb = 160;
+#ifdef ADALN_TUNING
+  // Tuning builds only (build.py --tuning): launch-shape sweeps.  The
+  // release library reads no environment variable.
   if (const char* env = getenv("ADALN_RING_KB")) {
     const int v = atoi(env);
     if (v >= 16 && v <= 256) ring_kb = v;
   }
+#endif
   int budget = ring_kb * 1024 / units;
   if (budget > per_team) budget = per_team;
   int stages = budget / stage_bytes;
@@ -329,11 +332,13 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, s->threads, s->smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  // ADALN_CTAS_PER_SM lowers the resident CTAs per SM (launch-shape sweeps).
+#ifdef ADALN_TUNING
+  // Tuning builds only: fewer resident CTAs per SM (launch-shape sweeps).
   if (const char* env = getenv("ADALN_CTAS_PER_SM")) {
     const int v = atoi(env);
     if (v >= 1 && v < per_sm) per_sm = v;
   }
+#endif
   int64_t g = (int64_t)sms * per_sm;
   if (g > T) g = T;
   s->grid = (int)(g < 1 ? 1 : g);
@@ -424,13 +429,15 @@ cudaError_t release_ticket(int slot, cudaStream_t st, bool launched) {
 
 // Device-wide units pay when a team's consecutive units rarely change
 // segment (a segment's modulation rows are reloaded at each change): when
-// segments are at least 4 rounds of all teams long.  ADALN_FWD_SCHED
-// (= "cta" or "device") forces either mode, for launch-shape sweeps.
+// segments are at least 4 rounds of all teams long.
 bool want_device_units(const FwdArgs& a, const Shape& s, int R) {
+#ifdef ADALN_TUNING
+  // Tuning builds only: ADALN_FWD_SCHED = "cta" or "device" forces a mode.
   if (const char* env = getenv("ADALN_FWD_SCHED")) {
     if (env[0] == 'c') return false;
     if (env[0] == 'd') return true;
   }
+#endif
   const int64_t round_rows = (int64_t)s.grid * s.teams * R;
   return a.T >= 2 * round_rows && a.T / a.nseg >= 4 * round_rows;
 }

@@ -9,11 +9,15 @@
 // (per-(CTA, segment) column partials).  This entry point takes that scratch
 // from a fixed file-scope device array instead, so it allocates nothing.
 //
-// The array lives in every GPU that loads this library, until the process
-// exits.  All calls on a device share it and it keeps the last call's
-// contents; the backward writes every partial slot it later reads, so nothing
-// needs clearing between calls.  Calls that overlap on the GPU (on different
-// streams, or from different threads) race on the array.
+// The array takes ADALN_NOALLOC_SCRATCH_BYTES of device memory on every GPU
+// where this file's module is loaded, until the process exits.  Under CUDA's
+// default lazy module loading that happens at the first adaln_bwd_noalloc
+// call on the device (its address lookup loads the module); with eager
+// loading (CUDA_MODULE_LOADING=EAGER) it happens when the library is first
+// used on the device.  All calls on a device share the array and it keeps the
+// last call's contents; the backward writes every partial slot it later
+// reads, so nothing needs clearing between calls.  Calls that overlap on the
+// GPU (on different streams, or from different threads) race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>

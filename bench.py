@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--rows", type=int, default=0,
+                   help="only the first ROWS tokens of the workload (a smaller case of the "
+                        "same structure, for profiler captures); 0 = all")
     p.add_argument("--sites", type=int, default=1,
                    help="modulation sites per step (mmdit_joint steady state: 60 = 2 per "
                         "block x 30 blocks), each its own shift/scale, back to back")
@@ -82,62 +85,183 @@ def peaks():
 
 
 # ---------------------------------------------------------------------------
-# Clock sampling during the timed region.
+# Clock record.  A thread samples the SM clock, the clock-event (throttle)
+# reasons and the power draw every ~1 ms through NVML (read-only queries,
+# libnvidia-ml via ctypes), or every 100 ms through nvidia-smi when NVML is
+# not loadable.  The main thread marks host-time windows (the timed loop, the
+# trace pass, the e2e leg); samples inside them are "under load".
 # ---------------------------------------------------------------------------
-class ClockSampler:
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+SMI_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class _Nvml:
+    """Minimal read-only NVML binding (clock, max clock, event reasons, power)."""
+
+    def __init__(self, pci_bus_id=None, uuid=None, index=None):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0 and uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        if rc != 0 and index is not None:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(int(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        mhz, mx, mw = ct.c_uint(0), ct.c_uint(0), ct.c_uint(0)
+        bits = ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.reasons_fn(self.h, ct.byref(bits))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        names = [n for b, n in REASON_BITS.items() if bits.value & b]
+        return float(mhz.value), float(mx.value), names, mw.value / 1000.0
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+def parse_smi_line(line):
+    """(sm_mhz, sm_max_mhz, reasons, power_w) from one nvidia-smi CSV line, or None."""
+    f = [x.strip() for x in line.split(",")]
+    if len(f) < 9:
+        return None
+    try:
+        sm, smax = float(f[1]), float(f[2])
+    except ValueError:
+        return None
+    try:
+        pw = float(f[3])
+    except ValueError:
+        pw = None
+    return sm, smax, [n for n, v in zip(SMI_REASONS, f[5:9]) if v.lower() == "active"], pw
+
+
+class ClockRecord:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, dev_ids=None, period_s=0.001):
+        self.ids = dev_ids or {}
+        self.period = period_s
+        self.samples = []   # (host time, sm_mhz, sm_max_mhz, reasons, power_w)
+        self.windows = []   # (name, t0, t1)
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
 
-    def __enter__(self):
+    # -- sampling ------------------------------------------------------------
+    def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.reader = threading.Thread(target=self._read, daemon=True)
-            self.reader.start()
-        except OSError:
-            self.proc = None
+            nv = _Nvml(self.ids.get("pci_bus_id"), self.ids.get("uuid"), self.ids.get("index"))
+        except (OSError, AttributeError):
+            nv = None
+        if nv is not None:
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._nvml_loop, args=(nv,), daemon=True)
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.ids.get("smi", 0)), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                return self
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+        self._thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _nvml_loop(self, nv):
+        try:
+            while not self._stop.is_set():
+                v = nv.sample()
+                if v is not None:
+                    self.samples.append((time.perf_counter(),) + v)
+                time.sleep(self.period)
+        finally:
+            nv.close()
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+    def _smi_loop(self):
+        for line in self._proc.stdout:
+            v = parse_smi_line(line)
+            if v is not None:
+                self.samples.append((time.perf_counter(),) + v)
+
+    def stop(self):
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.reader.join(timeout=2)
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    # -- windows ------------------------------------------------------------
+    def window(self, name):
+        rec = self
+
+        class _W:
+            def __enter__(self_):
+                self_.t0 = time.perf_counter()
+
+            def __exit__(self_, *exc):
+                rec.windows.append((name, self_.t0, time.perf_counter()))
+        return _W()
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        def inside(t, names=None):
+            return any(a <= t <= b for n, a, b in self.windows if names is None or n in names)
+        load = [s_ for s_ in self.samples if inside(s_[0])]
+        out = {"source": self.source, "samples": len(self.samples),
+               "samples_under_load": len(load),
+               "samples_by_window": {n: sum(1 for s_ in self.samples if inside(s_[0], (n,)))
+                                     for n in dict.fromkeys(w[0] for w in self.windows)}}
+        use = load or self.samples
+        if not use:
+            out.update(sm_mhz=None, sm_max_mhz=None, reasons=[], power_w_max=None)
+            return out
+        reasons = sorted({r for s_ in use for r in s_[3]})
+        pw = [s_[4] for s_ in use if s_[4] is not None]
+        out.update(sm_mhz=statistics.median(s_[1] for s_ in use),
+                   sm_mhz_min=min(s_[1] for s_ in use),
+                   sm_max_mhz=max(s_[2] for s_ in use), reasons=reasons,
+                   power_w_max=max(pw) if pw else None)
+        return out
+
+
+def device_ids(dev, local):
+    """Identifiers NVML can find the torch device by (PCI bus id, UUID, index)."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    ids = {"smi": gpu_smi_id(local)}
+    try:
+        ids["pci_bus_id"] = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        pass
+    u = str(getattr(p, "uuid", "") or "")
+    if u:
+        ids["uuid"] = u if u.startswith("GPU-") else "GPU-" + u
+    if ids["smi"].isdigit():
+        ids["index"] = int(ids["smi"])
+    return ids
 
 
 # ---------------------------------------------------------------------------
@@ -181,11 +305,19 @@ def max_over_ranks(pg, value, dev):
 # ---------------------------------------------------------------------------
 # Inputs.
 # ---------------------------------------------------------------------------
-def host_inputs(name):
+def host_inputs(name, rows=0):
+    """The workload's seeded inputs (one modulation site); with rows > 0 only
+    its first `rows` tokens and the segments they touch (a smaller case of
+    the same structure, e.g. for profiler captures)."""
     from adaln_video_dit_gb300 import inputs as I
     c = I.make(WORKLOADS[name])
     if isinstance(c["shift"], list):
         c["shift"], c["scale"] = c["shift"][0], c["scale"][0]
+    if 0 < rows < c["T"]:
+        nseg = int(c["seg_id"][rows - 1]) + 1
+        c.update(x=c["x"][:rows], dy=c["dy"][:rows], seg_id=c["seg_id"][:rows],
+                 shift=c["shift"][:nseg], scale=c["scale"][:nseg], T=rows, nseg=nseg,
+                 name=f"{c['name']}[:{rows}]")
     return c
 
 
@@ -237,6 +369,7 @@ def run_native(args, c, rank, local, world, pg):
         L.adaln_bwd(d["dy"], d["x"], mean, rstd, d["scale"], d["seg_id"], dx=dx,
                     dshift=dshift, dscale=dscale, workspace=ws, stream=stream)
 
+    clocks = ClockRecord(device_ids(dev, local)).start()
     for _ in range(args.warmup):
         evict_l2()
         fwd()
@@ -244,13 +377,14 @@ def run_native(args, c, rank, local, world, pg):
         bwd()
     rc, bits = L.adaln_get_status()
     if rc != L.ADALN_OK:
+        clocks.stop()
         raise RuntimeError(f"device status after warm-up: {L.strerror(rc)} ({bits})")
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_smi_id(local)) as clocks:
+    with clocks.window("timed"):
         for i in range(K):
             # L2 flushed before each call (not timed): inputs come from HBM.
             evict_l2()
@@ -270,12 +404,13 @@ def run_native(args, c, rank, local, world, pg):
     # timed steps above.
     KT = min(K, 500)
     L.adaln_trace_begin(3 * KT + 8)
-    for i in range(KT):
-        evict_l2()
-        fwd()
-        evict_l2()
-        bwd()
-    torch.cuda.synchronize(dev)
+    with clocks.window("trace"):
+        for i in range(KT):
+            evict_l2()
+            fwd()
+            evict_l2()
+            bwd()
+        torch.cuda.synchronize(dev)
     L.adaln_trace_end()
     rc, bits = L.adaln_get_status()
     if rc != L.ADALN_OK:
@@ -289,9 +424,10 @@ def run_native(args, c, rank, local, world, pg):
     for kid, name in L.KERNEL_NAMES.items():
         n, ms = L.adaln_trace_get(kid)
         kern[name] = dict(launches=n, avg_us=1000.0 * ms / n if n else None)
-    launches = 3 * K  # fwd, bwd row pass and finalize per timed step
+    launches = sum(n for n, _ in (L.adaln_trace_get(k) for k in L.KERNEL_NAMES)) * K // KT
 
-    e2e = run_e2e(args, c, h, dev, stream, L, tdt, pg)
+    e2e = run_e2e(args, c, h, dev, stream, L, tdt, pg, clocks)
+    clocks.stop()
     return dict(step_ms=step_ms, fwd_ms=statistics.mean(fwd_ms), bwd_ms=statistics.mean(bwd_ms),
                 fwd_ms_median=statistics.median(fwd_ms), bwd_ms_median=statistics.median(bwd_ms),
                 kernels=kern, launches=launches, clocks=clocks.summary(), e2e=e2e,
@@ -300,7 +436,7 @@ def run_native(args, c, rank, local, world, pg):
                 esize=esize)
 
 
-def run_e2e(args, c, h, dev, stream, L, tdt, pg):
+def run_e2e(args, c, h, dev, stream, L, tdt, pg, clocks):
     """Same step through the public host-buffer entry point
     (adaln_fwd_bwd_host): every step copies its inputs from pinned host memory
     to the device, runs fwd + bwd, and copies every result back, all inside
@@ -308,6 +444,8 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg):
     chunks over its own streams."""
     import torch
     T, D, nseg = c["T"], c["D"], c["nseg"]
+    if args.e2e_steps <= 0:
+        return None
     hin = {k: v.pin_memory() for k, v in h.items()}
     hout = dict(y=torch.empty(T, D, dtype=tdt).pin_memory(),
                 dx=torch.empty(T, D, dtype=tdt).pin_memory(),
@@ -328,11 +466,12 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg):
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with clocks.window("e2e"):
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     ms = max_over_ranks(pg, e0.elapsed_time(e1) / K, dev)
     bi = sum(v.numel() * v.element_size() for v in hin.values())
     bo = sum(v.numel() * v.element_size() for v in hout.values())
@@ -340,55 +479,76 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle timing (bounded sample of the same workload).
+# CPU oracle timing (bounded sample of the same workload): the forward, and the
+# backward from the forward's saved statistics, timed separately.
 # ---------------------------------------------------------------------------
-def oracle_step_fn(c, rows):
-    import oracle
+def oracle_sample(c, rows):
+    """The first `rows` tokens of the workload with the segments they touch."""
     sl = slice(0, rows)
     x, dy, seg = c["x"][sl], c["dy"][sl], c["seg_id"][sl]
     nseg = int(seg.max()) + 1 if rows else 1
-    sh, sc = c["shift"][:nseg], c["scale"][:nseg]
+    return x, dy, seg, c["shift"][:nseg], c["scale"][:nseg]
 
-    def step(nthreads):
-        oracle.adaln_fwd(x, sh, sc, seg, c["eps"], nthreads=nthreads)
-        oracle.adaln_bwd(dy, x, sc, seg, c["eps"], nthreads=nthreads)
-    return step
+
+def oracle_fwd_bwd_seconds(c, rows, nthreads):
+    """Seconds of one oracle forward and of one backward (from the forward's
+    mean/rstd, stored as fp32 like the library's) on the first `rows` tokens."""
+    import oracle
+    x, dy, seg, sh, sc = oracle_sample(c, rows)
+    t0 = time.perf_counter()
+    _, mean, rstd = oracle.adaln_fwd(x, sh, sc, seg, c["eps"], nthreads=nthreads)
+    t1 = time.perf_counter()
+    oracle.adaln_bwd(dy, x, sc, seg, c["eps"], mean=mean.astype(np.float32),
+                     rstd=rstd.astype(np.float32), nthreads=nthreads)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
 
 
 def time_oracle(c, seconds, nthreads):
-    """Tokens/s of the oracle's fwd+bwd on the first `rows` tokens of the
-    workload, `rows` grown until one call takes about `seconds`; when the
-    whole workload takes less, whole-workload calls are repeated until about
-    `seconds` have passed.  Returns (tokens/s, rows per call, seconds, calls)."""
+    """Time the oracle's forward and backward on the first `rows` tokens of
+    the workload, `rows` grown until one fwd + bwd takes about `seconds`;
+    when the whole workload takes less, whole-workload calls are repeated
+    until about `seconds` have passed.  Returns dict(rows, calls, fwd_s,
+    bwd_s) (seconds summed over the calls)."""
     rows = min(64, c["T"])
     while True:
-        step = oracle_step_fn(c, rows)
-        t0 = time.perf_counter()
-        step(nthreads)
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            return rows / dt, rows, dt, 1
+        tf, tb = oracle_fwd_bwd_seconds(c, rows, nthreads)
+        if tf + tb >= seconds:
+            return dict(rows=rows, calls=1, fwd_s=tf, bwd_s=tb)
         if rows >= c["T"]:
             calls = 1
-            while dt < seconds:
-                step(nthreads)
-                calls += 1
-                dt = time.perf_counter() - t0
-            return rows * calls / dt, rows, dt, calls
-        grow = max(2.0, min(8.0, 1.2 * seconds / max(dt, 1e-3)))
+            while tf + tb < seconds:
+                f, b = oracle_fwd_bwd_seconds(c, rows, nthreads)
+                tf, tb, calls = tf + f, tb + b, calls + 1
+            return dict(rows=rows, calls=calls, fwd_s=tf, bwd_s=tb)
+        grow = max(2.0, min(8.0, 1.2 * seconds / max(tf + tb, 1e-3)))
         rows = min(c["T"], int(rows * grow))
 
 
+def oracle_rates(r):
+    """Tokens/s of the forward, the backward and the fwd+bwd step."""
+    n = r["rows"] * r["calls"]
+    return {"fwd": n / r["fwd_s"], "bwd": n / r["bwd_s"], "fwd_bwd": n / (r["fwd_s"] + r["bwd_s"])}
+
+
 def cpu_baseline(c, seconds):
+    """The oracle on the host cores, all threads and one thread, for the
+    forward, the backward and the fwd+bwd step."""
     import oracle
     cores = oracle.hw_threads()
-    tps_mt, rows_mt, dt_mt, n_mt = time_oracle(c, seconds, cores)
-    tps_st, rows_st, dt_st, n_st = time_oracle(c, max(1.0, seconds / 4), 1)
-    return {"value": tps_mt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": (f"fp64 C++ oracle fwd+bwd on the first {rows_mt} tokens of the "
-                       f"workload, {n_mt} call(s) ({dt_mt:.1f} s, {cores} threads)"),
-            "single_thread": {"value": tps_st, "unit": "tokens/s", "cores": 1,
-                              "sample": f"first {rows_st} tokens, {n_st} call(s) ({dt_st:.1f} s)"}}
+    mt = time_oracle(c, seconds, cores)
+    st = time_oracle(c, max(1.0, seconds / 4), 1)
+    rm, rs = oracle_rates(mt), oracle_rates(st)
+
+    def sample(r, n):
+        return (f"fp64 C++ oracle on the first {r['rows']} of {c['T']} tokens, {r['calls']} "
+                f"call(s) of fwd then bwd ({r['fwd_s'] + r['bwd_s']:.1f} s, {n} thread(s))")
+    return {"value": rm["fwd_bwd"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample(mt, cores),
+            "modes": {k: {"threads": cores, "tokens_per_s": rm[k],
+                          "single_thread_tokens_per_s": rs[k]} for k in ("fwd", "bwd", "fwd_bwd")},
+            "single_thread": {"value": rs["fwd_bwd"], "unit": "tokens/s", "cores": 1,
+                              "sample": sample(st, 1)}}
 
 
 def gpu_smi_id(local):
@@ -407,36 +567,48 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import oracle
-    c = host_inputs(args.workload)
+    c = host_inputs(args.workload, args.rows)
     cores = oracle.hw_threads()
     # Size one step so that warm-up + timed steps take about two minutes.
     budget = 120.0 / max(1, args.steps + args.warmup)
-    probe = oracle_step_fn(c, min(64, c["T"]))
-    t0 = time.perf_counter()
-    probe(cores)
-    per_row = (time.perf_counter() - t0) / min(64, c["T"])
-    rows = int(max(1, min(c["T"], budget / max(per_row, 1e-9))))
-    step = oracle_step_fn(c, rows)
+    n0 = min(64, c["T"])
+    tf, tb = oracle_fwd_bwd_seconds(c, n0, cores)
+    rows = int(max(1, min(c["T"], budget / max((tf + tb) / n0, 1e-9))))
     for _ in range(args.warmup):
-        step(cores)
-    t0 = time.perf_counter()
+        oracle_fwd_bwd_seconds(c, rows, cores)
+    sf = sb = 0.0
     for _ in range(args.steps):
-        step(cores)
-    dt = time.perf_counter() - t0
+        f, b = oracle_fwd_bwd_seconds(c, rows, cores)
+        sf, sb = sf + f, sb + b
+    dt = sf + sb
     value = rows * args.steps / dt
-    sample = (f"fp64 C++ oracle fwd+bwd on the first {rows} of {c['T']} tokens per step, "
+    sample = (f"fp64 C++ oracle fwd then bwd on the first {rows} of {c['T']} tokens per step, "
               f"{cores} threads")
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"], "data": "synthetic",
-           "config": {"workload": c["name"], "T": c["T"], "D": c["D"], "nseg": c["nseg"],
-                      "tokens_per_step": rows},
+           "config": bench_config(c, world),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                            "kind": "oracle", "sample": sample},
+                            "kind": "oracle", "sample": sample,
+                            "modes": {"fwd": {"threads": cores,
+                                              "tokens_per_s": rows * args.steps / sf},
+                                      "bwd": {"threads": cores,
+                                              "tokens_per_s": rows * args.steps / sb}},
+                            "tokens_per_step": rows},
            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def bench_config(c, world):
+    """The workload description both arms print (identical keys and values)."""
+    es = 2 if c["dtype"] == "bf16" else 4
+    return {"workload": c["name"], "T": c["T"], "D": c["D"], "nseg": c["nseg"],
+            "io_dtype": c["dtype"], "accumulate": "f32",
+            "l2": "inputs larger than L2 (x, dy %d MiB each); L2 also evicted before every "
+                  "call by an untimed read of 2x L2" % (c["T"] * c["D"] * es >> 20),
+            "parallelism": f"replicas x{world} (no data-path collective)"}
 
 
 def load_traffic(kernel):
@@ -520,7 +692,8 @@ def run_sites(args, rank, local, world, pg):
     ms = []
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_smi_id(local)) as clocks:
+    clocks = ClockRecord(device_ids(dev, local)).start()
+    with clocks.window("timed"):
         for _ in range(K):
             torch.sum(flush, dim=0, out=flush_out)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -532,6 +705,7 @@ def run_sites(args, rank, local, world, pg):
             e1.record(stream)
             ms.append((e0, e1))
         torch.cuda.synchronize(dev)
+    clocks.stop()
     barrier(pg, dev)
     step_ms = max_over_ranks(pg, statistics.mean(a.elapsed_time(b) for a, b in ms), dev)
     if rank == 0:
@@ -697,7 +871,7 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
-    c = host_inputs(args.workload)
+    c = host_inputs(args.workload, args.rows)
     r = run_native(args, c, rank, local, world, pg)
     if rank == 0:
         T, D, nseg, es = c["T"], c["D"], c["nseg"], r["esize"]
@@ -722,12 +896,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["step_ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": c["dtype"], "data": "synthetic",
-            "config": {"workload": c["name"], "T": T, "D": D, "nseg": nseg,
-                       "io_dtype": c["dtype"], "accumulate": "f32",
-                       "l2": "inputs larger than L2 (x, dy %d MiB each); L2 also evicted "
-                             "before every call by an untimed read of 2x L2" % (T * D * es >> 20),
-                       "parallelism": f"replicas x{world} (no data-path collective)",
-                       "launch_fwd": r["shape_fwd"], "launch_bwd_rows": r["shape_bwd"]},
+            "config": bench_config(c, world),
+            "launch": {"fwd": r["shape_fwd"], "bwd_rows": r["shape_bwd"]},
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "traffic_note": traffic_note,
@@ -736,11 +906,15 @@ def main():
             "kernels": r["kernels"],
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
-            "e2e": {"value": world * T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                    "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
-                    "api": "adaln_fwd_bwd_host"},
+            "e2e": None if e2e is None else {
+                "value": world * T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
+                "api": "adaln_fwd_bwd_host"},
         }
+        if r["clocks"].get("sm_mhz"):
+            # Clock-normalised cost of a step: its time in SM clock cycles.
+            out["clocks"]["step_mcycles"] = r["step_ms"] * 1e-3 * r["clocks"]["sm_mhz"]
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
         print(json.dumps(out), flush=True)

@@ -117,10 +117,12 @@ ADALN_API int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg,
  * fp32 sequence reductions dshift, dscale [nseg, D].  Two kernel launches on
  * `stream`: a row pass that also accumulates per-(CTA, segment) column
  * partials into `workspace`, then a fixed-order reduction of those partials.
- * No floating-point atomics: for a given device and sizes the results are
- * bitwise reproducible.  `workspace` (>= adaln_bwd_workspace_size bytes,
- * 16-byte aligned) is scratch owned by the caller; its contents on entry do
- * not matter.  Calls sharing one workspace must not overlap on the device.
+ * No floating-point atomics: for a given device and sizes the results of
+ * valid input are bitwise reproducible.  (With an invalid seg_id the outputs
+ * are unspecified and may differ between runs: teams whose clamped segment
+ * paths cross can share a partial slot.)  `workspace` (at least
+ * adaln_bwd_workspace_size bytes, 16-byte aligned) is scratch owned by the
+ * caller; its contents on entry do not matter.  Calls sharing one workspace must not overlap on the device.
  * A NULL workspace is ADALN_ERR_NULL (adaln_bwd_noalloc serves callers
  * without one); a short one is ADALN_ERR_WORKSPACE.
  */
@@ -137,10 +139,13 @@ ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
  * synchronise the device).  The paper has no counterpart: this is a
  * deployment variant of adaln_bwd.  Same arguments, results and launches as
  * adaln_bwd, minus the workspace: the scratch is a fixed file-scope device
- * array of ADALN_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the
- * library until the process exits.  Sizes whose adaln_bwd_workspace_size
- * exceeds it are rejected with ADALN_ERR_WORKSPACE before anything is
- * launched.  The first call on a device looks up the array's device address
+ * array of ADALN_NOALLOC_SCRATCH_BYTES.  A device holds it from the first
+ * adaln_bwd_noalloc call on it (under CUDA's default lazy module loading;
+ * from the library's first use there under eager loading) until the process
+ * exits.  The partials grow with the SM count (G = SMs x teams per SM):
+ * 3072-wide bf16 rows with 822 segments fit up to 181 SMs.  Sizes whose
+ * adaln_bwd_workspace_size exceeds it are rejected with ADALN_ERR_WORKSPACE
+ * before anything is launched.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls on a device share the array and it
  * keeps the last call's contents (nothing in it needs to start at zero);

@@ -90,12 +90,57 @@ def sample_rows(T, grid, n_random=512, seed=0):
     return np.array(sorted(rows), np.int64)
 
 
+# Guard bands (the stand-in for a memory checker, which this GPU pool does not
+# offer): every output and the workspace live inside a larger buffer whose
+# bytes outside the stated extent hold CANARY; any write past either end
+# changes them.
+CANARY = 0xA5
+PAD = 4096  # bytes before and after; keeps the 16-byte alignment of the view
+
+
+def guarded_empty(shape, dtype, dev="cuda"):
+    """(raw uint8 buffer, view of `shape`/`dtype` inside it, PAD bytes in)."""
+    n = 1
+    for s_ in shape:
+        n *= int(s_)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    raw = torch.full((nbytes + 2 * PAD,), CANARY, dtype=torch.uint8, device=dev)
+    return raw, raw[PAD:PAD + nbytes].view(dtype).view(*shape)
+
+
+def check_guards(guards):
+    """Assert that no byte outside any guarded view was written."""
+    torch.cuda.synchronize()
+    for name, raw in guards.items():
+        lo, hi = raw[:PAD], raw[-PAD:]
+        bad_lo = int((lo != CANARY).sum())
+        bad_hi = int((hi != CANARY).sum())
+        assert bad_lo == 0 and bad_hi == 0, \
+            f"{name}: {bad_lo} bytes before and {bad_hi} bytes after the extent were written"
+
+
 def run_gpu(d, eps, workspace=None, stream=None):
+    """Forward then backward through the C ABI; every output (and the
+    workspace, unless one is given) sits inside a guard band that is checked
+    after the calls."""
     L = lib()
-    y, mean, rstd = L.adaln_fwd(d["x"], d["shift"], d["scale"], d["seg_id"], eps, stream=stream)
-    dx, dshift, dscale = L.adaln_bwd(d["dy"], d["x"], mean, rstd, d["scale"], d["seg_id"],
-                                     workspace=workspace, stream=stream)
-    return dict(y=y, mean=mean, rstd=rstd, dx=dx, dshift=dshift, dscale=dscale)
+    T, D = d["x"].shape
+    nseg = d["shift"].shape[0]
+    dt = d["x"].dtype
+    g, out = {}, {}
+    for k, shape, t in (("y", (T, D), dt), ("dx", (T, D), dt), ("mean", (T,), torch.float32),
+                        ("rstd", (T,), torch.float32), ("dshift", (nseg, D), torch.float32),
+                        ("dscale", (nseg, D), torch.float32)):
+        g[k], out[k] = guarded_empty(shape, t)
+    if workspace is None:
+        g["workspace"], workspace = guarded_empty(
+            (max(16, L.adaln_bwd_workspace_size(T, D, nseg, dt)),), torch.uint8)
+    L.adaln_fwd(d["x"], d["shift"], d["scale"], d["seg_id"], eps, y=out["y"], mean=out["mean"],
+                rstd=out["rstd"], stream=stream)
+    L.adaln_bwd(d["dy"], d["x"], out["mean"], out["rstd"], d["scale"], d["seg_id"], dx=out["dx"],
+                dshift=out["dshift"], dscale=out["dscale"], workspace=workspace, stream=stream)
+    check_guards(g)
+    return out
 
 
 def check_against_oracle(c, d, out, rows=None):
