@@ -98,6 +98,17 @@ cudaError_t status_ptr(unsigned** out) {
   return cudaSuccess;
 }
 
+// ----- launch slots ----------------------------------------------------------
+struct SlotPool {
+  cudaEvent_t ev[kLaunchSlots] = {};
+  bool recorded[kLaunchSlots] = {};
+  bool pending[kLaunchSlots] = {};  // handed out, event not yet recorded
+  unsigned gen[kLaunchSlots] = {};
+  int cursor = 0;
+};
+std::mutex g_slot_mu;
+SlotPool g_slot_pools[kNumSlotPools][kMaxDevices];
+
 // ----- timing trace -----------------------------------------------------------
 struct TraceRec {
   int kernel;
@@ -139,6 +150,53 @@ int cuda_fail(cudaError_t e) {
 }  // namespace
 
 namespace adaln {
+
+int launch_slot_acquire(int pool, cudaStream_t st, unsigned* generation) {
+  if (pool < 0 || pool >= kNumSlotPools) return -1;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  std::lock_guard<std::mutex> lk(g_slot_mu);
+  SlotPool& p = g_slot_pools[pool][dev];
+  for (int i = 0; i < kLaunchSlots; ++i) {
+    const int slot = (p.cursor + i) % kLaunchSlots;
+    if (p.pending[slot]) continue;
+    if (p.recorded[slot]) {
+      const cudaError_t q = cudaEventQuery(p.ev[slot]);
+      if (q == cudaErrorNotReady) continue;
+      if (q != cudaSuccess) return -1;
+    } else if (p.ev[slot] == nullptr &&
+               cudaEventCreateWithFlags(&p.ev[slot], cudaEventDisableTiming) != cudaSuccess) {
+      return -1;
+    }
+    p.pending[slot] = true;
+    p.cursor = (slot + 1) % kLaunchSlots;
+    if (++p.gen[slot] == 0) p.gen[slot] = 1;
+    if (generation) *generation = p.gen[slot];
+    return slot;
+  }
+  return -1;
+}
+
+cudaError_t launch_slot_release(int pool, int slot, cudaStream_t st, bool launched) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_slot_mu);
+  SlotPool& p = g_slot_pools[pool][dev];
+  p.pending[slot] = false;
+  if (!launched) return cudaSuccess;
+  e = cudaEventRecord(p.ev[slot], st);
+  if (e == cudaSuccess)
+    p.recorded[slot] = true;
+  else
+    p.pending[slot] = true;  // completion unknown: never hand it out again
+  return e;
+}
 
 int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* seg_id,
             int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, float eps, void* y,

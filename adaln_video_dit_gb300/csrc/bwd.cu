@@ -403,8 +403,7 @@ void* rows_kernel_for_v(bool exact) {
 template <class E>
 void* rows_kernel_for(int variant, bool exact) {
   switch (variant) {
-    case 0: return rows_kernel_for_v<E, 0>(exact);
-    case 1: return rows_kernel_for_v<E, 1>(exact);
+    case 6: return rows_kernel_for_v<E, 6>(exact);
     case 2: return rows_kernel_for_v<E, 2>(exact);
     case 4: return rows_kernel_for_v<E, 4>(exact);
     default: return rows_kernel_for_v<E, 3>(exact);
@@ -436,7 +435,8 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {
   // Slot groups per column: about 4-8 partials per group for the longest
-  // segments (power of two, 1..64), a single group when segments are short.
+  // segments (power of two, 1..64; one round of 8 loads in flight per
+  // thread), a single group when segments are short.
   const int64_t per_seg = (virtual_ctas(s) + a.nseg - 1) / a.nseg;
   int gpc = 1;
   while (gpc < 64 && per_seg > 8 * gpc) gpc *= 2;

@@ -160,6 +160,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return done != 0;
 }
 
+// Longest wait of a producer for its first stage's copies to land before it
+// issues the next stage's (a head start for the first stages of all teams).
+constexpr uint64_t kFirstStageHeadNs = 3000;
+
 // Suspend hint of the waits below: long enough that a waiting thread sleeps
 // instead of spinning (taking issue slots from the other warps), short
 // enough that the abort flag and the time bound are still polled.

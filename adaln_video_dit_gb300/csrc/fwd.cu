@@ -254,7 +254,7 @@ void* fwd_kernel_for_v(bool exact) {
 template <class E>
 void* fwd_kernel_for(int variant, bool exact) {
   switch (variant) {
-    case 0: return fwd_kernel_for_v<E, 0>(exact);
+    case 5: return fwd_kernel_for_v<E, 5>(exact);
     case 1: return fwd_kernel_for_v<E, 1>(exact);
     case 2: return fwd_kernel_for_v<E, 2>(exact);
     default: return fwd_kernel_for_v<E, 3>(exact);
@@ -342,6 +342,7 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   int64_t g = (int64_t)sms * per_sm;
   if (g > T) g = T;
   s->grid = (int)(g < 1 ? 1 : g);
+  s->sms = sms;
   return cudaSuccess;
 }
 
@@ -353,78 +354,32 @@ cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
                        variant_min_blocks(v), kCtaHeaderBytes, s);
 }
 
-// Device-wide unit counters {next unit, producers done}, one slot per launch
-// in flight.  Zero at module load; the last producer of a launch zeroes its
-// slot again.  A slot is handed to a launch only when the launch that used it
-// before has completed (its event), so no two running launches share one.
-constexpr int kTicketSlots = 256;
-__device__ int g_fwd_tickets[kTicketSlots][2];
+// Device-wide unit counters {next unit, producers done}, one per launch slot
+// (internal.h): zero at module load; the last producer of a launch zeroes its
+// counters again, and a slot is handed to a launch only when the launch that
+// used it before has completed.
+__device__ int g_fwd_tickets[kLaunchSlots][2];
 
 namespace {
 
-struct TicketPool {
-  bool ready = false;
-  int* base = nullptr;
-  cudaEvent_t ev[kTicketSlots] = {};
-  bool recorded[kTicketSlots] = {};
-  bool pending[kTicketSlots] = {};  // handed out, event not yet recorded
-  int cursor = 0;
-};
-constexpr int kMaxTicketDevices = 64;
-std::mutex g_ticket_mu;
-TicketPool g_tickets[kMaxTicketDevices];
-
-// A free slot for a launch on `st`, or -1 (then the launch uses CTA-local
-// units).  Launches being captured into a graph get none: a graph may be
-// replayed while other work runs, so it cannot hold a slot.
-int acquire_ticket(cudaStream_t st, int** ptr) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
-    return -1;
+// Device address of g_fwd_tickets on the current device (looked up once per
+// device), or nullptr.
+int* fwd_tickets_base() {
+  constexpr int kDevices = 64;
+  static std::mutex mu;
+  static int* base[kDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxTicketDevices) return -1;
-  std::lock_guard<std::mutex> lk(g_ticket_mu);
-  TicketPool& p = g_tickets[dev];
-  if (!p.ready) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!base[dev]) {
     void* b = nullptr;
-    if (cudaGetSymbolAddress(&b, g_fwd_tickets) != cudaSuccess) return -1;
-    p.base = static_cast<int*>(b);
-    p.ready = true;
-  }
-  for (int i = 0; i < kTicketSlots; ++i) {
-    const int slot = (p.cursor + i) % kTicketSlots;
-    if (p.pending[slot]) continue;
-    if (p.recorded[slot]) {
-      const cudaError_t q = cudaEventQuery(p.ev[slot]);
-      if (q == cudaErrorNotReady) continue;
-      if (q != cudaSuccess) return -1;
-    } else if (p.ev[slot] == nullptr &&
-               cudaEventCreateWithFlags(&p.ev[slot], cudaEventDisableTiming) != cudaSuccess) {
-      return -1;
+    if (cudaGetSymbolAddress(&b, g_fwd_tickets) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
     }
-    p.pending[slot] = true;
-    p.cursor = (slot + 1) % kTicketSlots;
-    *ptr = p.base + 2 * slot;
-    return slot;
+    base[dev] = static_cast<int*>(b);
   }
-  return -1;
-}
-
-// After the launch: the slot is busy until the work now queued on `st` ends.
-cudaError_t release_ticket(int slot, cudaStream_t st, bool launched) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lk(g_ticket_mu);
-  TicketPool& p = g_tickets[dev];
-  p.pending[slot] = false;
-  if (!launched) return cudaSuccess;
-  e = cudaEventRecord(p.ev[slot], st);
-  if (e == cudaSuccess)
-    p.recorded[slot] = true;
-  else
-    p.pending[slot] = true;  // completion unknown: never hand it out again
-  return e;
+  return base[dev];
 }
 
 // Device-wide units pay when a team's consecutive units rarely change
@@ -451,11 +406,15 @@ cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
   FwdArgs args = a;
   args.ticket = nullptr;
   int slot = -1;
-  if (want_device_units(a, s, fwd_rows(s.variant))) slot = acquire_ticket(st, &args.ticket);
+  if (want_device_units(a, s, fwd_rows(s.variant))) {
+    int* base = fwd_tickets_base();
+    if (base) slot = launch_slot_acquire(kPoolFwdUnits, st, nullptr);
+    if (slot >= 0) args.ticket = base + 2 * slot;
+  }
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
   const cudaError_t e = cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
   if (slot >= 0) {
-    const cudaError_t r = release_ticket(slot, st, e == cudaSuccess);
+    const cudaError_t r = launch_slot_release(kPoolFwdUnits, slot, st, e == cudaSuccess);
     if (e == cudaSuccess && r != cudaSuccess) return r;
   }
   return e;

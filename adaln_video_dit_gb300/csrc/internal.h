@@ -29,33 +29,38 @@ constexpr int kCtaHeaderBytes = 128;
 
 // Compiled variants of the staging kernels, chosen by the row length in
 // 16-byte vectors (nvec): vectors per thread (VPT), the largest consumer-warp
-// count, and the CTAs per SM the register budget is sized for.  At most 8
-// consumer warps share a row, so the per-row reduction work (shuffles, one
-// shared-memory exchange, scalar statistics) is repeated by few warps.  The
-// register cap follows from the warps per SM sub-partition: 14 warps per SM
-// (7 x 2 CTAs) allow 128 registers a thread, 12 or 9 warps allow 168.
-//   variant 0: nvec <=  192  VPT 1, <= 6 warps, 2 CTAs/SM
-//   variant 1: nvec <=  384  VPT 2, <= 6 warps, 2 CTAs/SM
-//   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 CTAs/SM
-//   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 CTA/SM
-//   variant 4: nvec <=  384  VPT 4, <= 3 warps, 3 CTAs/SM (backward only:
-//              its column sums favour few warps per row, many rows per SM)
+// count, and the teams per SM the register budget is sized for (one CTA per
+// SM holds them).  At most 8 consumer warps share a row, so the per-row
+// reduction work (shuffles, one shared-memory exchange, scalar statistics) is
+// repeated by few warps; short rows use few warps per row and more teams, so
+// that per-row overheads are shared by more elements.  The register cap
+// follows from the warps per SM: 12 or 9 warps allow 168 registers a thread,
+// 16 allow 128.
+//   variant 5: nvec <=  192  VPT 2, <= 3 warps, 4 teams (forward)
+//   variant 6: nvec <=  192  VPT 2, <= 3 warps, 3 teams (backward)
+//   variant 1: nvec <=  384  VPT 2, <= 6 warps, 2 teams (forward)
+//   variant 4: nvec <=  384  VPT 4, <= 3 warps, 3 teams (backward: its column
+//              sums favour few warps per row, many rows per SM)
+//   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 teams
+//   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 team
 ADALN_HD inline int choose_variant(int nvec) {
-  return nvec <= 192 ? 0 : (nvec <= 384 ? 1 : (nvec <= 640 ? 2 : 3));
+  return nvec <= 192 ? 5 : (nvec <= 384 ? 1 : (nvec <= 640 ? 2 : 3));
 }
 ADALN_HD inline int choose_bwd_variant(int nvec) {
-  return nvec <= 192 ? 0 : (nvec <= 384 ? 4 : (nvec <= 640 ? 2 : 3));
+  return nvec <= 192 ? 6 : (nvec <= 384 ? 4 : (nvec <= 640 ? 2 : 3));
 }
-ADALN_HD constexpr int variant_vpt(int v) { return v == 0 ? 1 : (v == 1 ? 2 : 4); }
+ADALN_HD constexpr int variant_vpt(int v) { return (v == 1 || v == 5 || v == 6) ? 2 : 4; }
 ADALN_HD constexpr int variant_max_warps(int v) {
-  return v == 2 ? 5 : (v == 3 ? 8 : (v == 4 ? 3 : 6));
+  return v == 2 ? 5 : (v == 3 ? 8 : ((v == 4 || v == 5 || v == 6) ? 3 : 6));
 }
-ADALN_HD constexpr int variant_min_blocks(int v) { return v == 3 ? 1 : (v == 4 ? 3 : 2); }
+ADALN_HD constexpr int variant_min_blocks(int v) {
+  return v == 3 ? 1 : ((v == 4 || v == 6) ? 3 : (v == 5 ? 4 : 2));
+}
 ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
 // Rows per reduction round.  A round's latency hardly depends on the row
 // length, so short rows take more rows per round (as registers allow).
-ADALN_HD constexpr int fwd_rows(int v) { return v == 0 ? 8 : 4; }
-ADALN_HD constexpr int bwd_rows(int v) { return v == 0 ? 4 : 2; }
+ADALN_HD constexpr int fwd_rows(int v) { return v == 5 ? 8 : 4; }
+ADALN_HD constexpr int bwd_rows(int v) { return v == 6 ? 4 : 2; }
 // The row fills the variant's largest consumer-warp count exactly.
 ADALN_HD inline bool variant_exact(int v, int nvec) {
   return nvec == variant_max_warps(v) * 32 * variant_vpt(v);
@@ -72,6 +77,7 @@ struct Shape {
   int stages;     // depth of the shared-memory ring
   int smem;       // dynamic shared memory bytes
   int grid;       // persistent CTAs
+  int sms;        // SMs of the device
   int nvec;       // 16-byte vectors per row
   int row_bytes;  // bytes of one row of x
 };
@@ -155,6 +161,20 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
             size_t workspace_bytes, cudaStream_t st, int accumulate);
 size_t bwd_workspace_need(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, int* rc);
 int check_dims_public(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dt);
+
+// Launch slots (api.cu).  A launch that needs device-wide state of its own
+// (the forward's unit counters) takes one of kLaunchSlots slots of a pool and
+// indexes a static device array with it.  A slot is handed out only when the
+// launch that used it before has completed (a CUDA event per slot), so no two
+// launches in flight share one; launches being captured into a CUDA graph get
+// none (a graph may be replayed while other work runs).  Each acquisition
+// also returns the slot's generation, counting its uses from 1.
+constexpr int kLaunchSlots = 256;
+enum { kPoolFwdUnits = 0, kNumSlotPools = 1 };
+// A slot index, or -1 when none is free (or the stream is capturing).
+int launch_slot_acquire(int pool, cudaStream_t st, unsigned* generation);
+// After the launch: the slot stays busy until the work queued on `st` ends.
+cudaError_t launch_slot_release(int pool, int slot, cudaStream_t st, bool launched);
 
 // Bounded-wait self-test (selftest.cu).
 cudaError_t launch_wait_timeout_probe(unsigned* status, uint64_t limit_ns, cudaStream_t st);

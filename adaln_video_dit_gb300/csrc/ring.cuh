@@ -104,6 +104,14 @@ __device__ __forceinline__ void ring_produce(const Ring& rg,
       bulk_g2s(dst + (uint32_t)i * R * row_bytes,
                src[i] + (size_t)k * R * row_bytes, bytes, rg.full(s), policy);
     issued = k + 1;
+    if (k == 0) {
+      // Every team issues its whole ring at once at the start; let the first
+      // stage's copies go ahead of the next ones, so that the first round can
+      // start early: wait, briefly and bounded, for them to land.
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(rg.full(0), 0) && globaltimer_ns() - t0 < kFirstStageHeadNs) {
+      }
+    }
   }
   // Drain: the newest chunk of each stage is the only one possibly in flight.
   for (int s = 0; s < S; ++s) {

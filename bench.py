@@ -462,6 +462,19 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg, clocks):
 
     for _ in range(3):
         step()
+    # The host link bounds this leg: its copy rate on this machine, each way alone
+    # (pinned memory, one copy of x), for reading the e2e number.
+    probe = torch.empty_like(hin["x"], device=dev)
+    link = {}
+    for name, dst, src in (("h2d_gbs", probe, hin["x"]), ("d2h_gbs", hout["y"], probe)):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dst.copy_(src, non_blocking=True)
+        a_.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        link[name] = src.numel() * src.element_size() / (a_.elapsed_time(b_) * 1e-3) / 1e9
+    del probe
     K = args.e2e_steps
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
@@ -475,7 +488,7 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg, clocks):
     ms = max_over_ranks(pg, e0.elapsed_time(e1) / K, dev)
     bi = sum(v.numel() * v.element_size() for v in hin.values())
     bo = sum(v.numel() * v.element_size() for v in hout.values())
-    return dict(ms_per_step=ms, h2d=bi, d2h=bo, steps=K)
+    return dict(ms_per_step=ms, h2d=bi, d2h=bo, steps=K, link=link)
 
 
 # ---------------------------------------------------------------------------
@@ -910,7 +923,10 @@ def main():
                 "value": world * T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
-                "api": "adaln_fwd_bwd_host"},
+                "api": "adaln_fwd_bwd_host",
+                "host_link_gbs": e2e["link"],
+                "link_bound_ms": 1e3 * max(e2e["h2d"] / (e2e["link"]["h2d_gbs"] * 1e9),
+                                           e2e["d2h"] / (e2e["link"]["d2h_gbs"] * 1e9))},
         }
         if r["clocks"].get("sm_mhz"):
             # Clock-normalised cost of a step: its time in SM clock cycles.

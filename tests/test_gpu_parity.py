@@ -63,7 +63,8 @@ EDGE = [
     (7, 8, 3, "bf16", [0, 7, 0]),          # T below the grid; empty first/last segment
     (1001, 136, 5, "bf16", None),          # ragged: odd T, nvec = 17
     (999, 24, 4, "f32", [1, 1, 1, 996]),   # one-row segments, nvec = 6
-    (300, 1536, 2, "bf16", None),          # nvec 192: variant 0 (VPT 1), 6 warps
+    (300, 1536, 2, "bf16", None),          # nvec 192: variants 5/6 (VPT 2), 3 warps
+    (300, 1528, 2, "bf16", None),          # nvec 191: variants 5/6, ragged last vector
     (300, 1544, 2, "bf16", None),          # nvec 193: variant 1 (VPT 2), 4 warps, ragged
     (300, 3072, 3, "bf16", None),          # nvec 384: variant 1, 6 warps
     (300, 3080, 3, "bf16", None),          # nvec 385: variant 2 (VPT 4), 4 warps, ragged
@@ -238,10 +239,10 @@ def test_launch_shape_matches_the_rules(adaln):
     assert s["grid"] == 3 and s["threads"] == 2 * 6 * 32
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 1, 5120, 1, torch.bfloat16)
     assert s["grid"] == 1 and s["threads"] == 6 * 32
-    # D = 1536 bf16: 192 vectors, 1 per thread -> 6 consumer warps; the
-    # forward runs one CTA per SM with two teams of 6 + 1 warps.
+    # D = 1536 bf16: 192 vectors, 2 per thread -> 3 consumer warps; the
+    # forward runs one CTA per SM with four teams of 3 + 1 warps.
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 8192, 1536, 2, torch.bfloat16)
-    assert s["threads"] == 2 * 7 * 32 and s["grid"] == sms
+    assert s["threads"] == 4 * 4 * 32 and s["grid"] == sms
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 5, 5120, 1, torch.bfloat16)
     assert s["grid"] == 5
 
@@ -279,3 +280,4 @@ def test_cuda_graph_capture_matches_eager(adaln):
     torch.cuda.synchronize()
     for k in ref:
         assert torch.equal(out[k], ref[k]), k
+
