@@ -440,6 +440,15 @@ cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t s
   const int64_t per_seg = (virtual_ctas(s) + a.nseg - 1) / a.nseg;
   int gpc = 1;
   while (gpc < 64 && per_seg > 8 * gpc) gpc *= 2;
+  // The blocks start only as the row pass frees SMs, 4 per SM: when the grid
+  // would need a second wave, and half the groups (two rounds of loads per
+  // thread) would not, take half.
+  auto blocks = [&](int g) {
+    const int64_t cb = kFinalizeThreads / g;
+    return (int64_t)a.nseg * ((2 * (a.D / 4) + cb - 1) / cb);
+  };
+  if (gpc > 1 && blocks(gpc) > 4 * (int64_t)s.sms && blocks(gpc / 2) <= 4 * (int64_t)s.sms)
+    gpc /= 2;
   int G = (int)virtual_ctas(s);
   BwdArgs args = a;
   void* params[] = {&args, &G, &gpc};

@@ -88,7 +88,10 @@ def m_comp_for_step_time(a, b, tau):
 def shape_benchmark(shapes, D=5120, steps=20, warmup=3, seed=0):
     """Time the fused AdaLN forward + backward (bf16, on the current CUDA
     device) for each (B, S) in `shapes`; one segment per sample.  Returns a
-    list of (B, S, ms).  Needs a GPU and libadaln.so."""
+    list of (B, S, ms): GPU time per step of back-to-back steps.  Outputs and
+    workspace are allocated once, and the steps are queued behind a short
+    device-side delay, so the host's per-call time is never on the measured
+    path.  Needs a GPU and libadaln.so."""
     import torch
 
     from . import _lib as L
@@ -105,14 +108,21 @@ def shape_benchmark(shapes, D=5120, steps=20, warmup=3, seed=0):
         seg = sample_seg_ids(B, S, device="cuda")
         ws = torch.empty(L.adaln_bwd_workspace_size(T, D, B, torch.bfloat16), device="cuda",
                          dtype=torch.uint8)
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        m = torch.empty(T, device="cuda")
+        r = torch.empty(T, device="cuda")
+        dsh = torch.empty(B, D, device="cuda")
+        dsc = torch.empty(B, D, device="cuda")
 
         def step():
-            y, m, r = L.adaln_fwd(x, mod, mod, seg, 1e-6)
-            L.adaln_bwd(dy, x, m, r, mod, seg, workspace=ws)
+            L.adaln_fwd(x, mod, mod, seg, 1e-6, y=y, mean=m, rstd=r)
+            L.adaln_bwd(dy, x, m, r, mod, seg, dx=dx, dshift=dsh, dscale=dsc, workspace=ws)
 
         for _ in range(warmup):
             step()
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e7))  # ~10 ms: the host queues every step meanwhile
         e0.record()
         for _ in range(steps):
             step()

@@ -56,10 +56,11 @@ def parse_args():
                         "block x 30 blocks), each its own shift/scale, back to back")
     p.add_argument("--graph", action="store_true",
                    help="with --sites: replay each step as one captured CUDA graph")
-    p.add_argument("--report", choices=["unfused", "shapes"], default=None,
+    p.add_argument("--report", choices=["unfused", "shapes", "fixed-cost"], default=None,
                    help="instead of the benchmark line: compare with torch's unfused "
-                        "chain (time and saved activation bytes), or shape-benchmark "
-                        "the operator and fit the step-time cost model")
+                        "chain (time and saved activation bytes), shape-benchmark the "
+                        "operator and fit the step-time cost model, or split a call's "
+                        "fixed cost into host and GPU time")
     return p.parse_args()
 
 
@@ -766,6 +767,116 @@ def report_shapes(args):
         "b_shape": {str(k): v for k, v in buckets.items()}}))
 
 
+def report_fixed_cost(args):
+    """Where a call's time goes, host or GPU, per workload: host time of one
+    call through the C ABI (the raw ctypes call and the Python binding with
+    outputs given), GPU time between CUDA events per call with the host kept
+    ahead of the GPU (a device-side delay first, so no launch waits for the
+    host), the library's per-kernel trace, and the floor of any call timed
+    this way (a one-element fill between the same events).  L2 evicted
+    before every call."""
+    import ctypes
+    import torch
+    from adaln_video_dit_gb300 import _lib as L
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, device=dev)
+    fo = torch.empty((), device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    S = ctypes.c_void_p(st.cuda_stream)
+    K = 40
+
+    def gpu_us(f, b):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(int(1e8))  # the host queues every call meanwhile
+        for e in ev:
+            torch.sum(flush, dim=0, out=fo)
+            e[0].record(st)
+            f()
+            e[1].record(st)
+            torch.sum(flush, dim=0, out=fo)
+            e[2].record(st)
+            b()
+            e[3].record(st)
+        torch.cuda.synchronize(dev)
+        return (statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev),
+                statistics.median(e[2].elapsed_time(e[3]) * 1e3 for e in ev))
+
+    def host_us(fn, n=200):
+        torch.cuda._sleep(int(4e8))
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        dt = (time.perf_counter() - t0) / n * 1e6
+        torch.cuda.synchronize(dev)
+        return dt
+
+    tiny = torch.empty(1, device=dev)
+    floor = gpu_us(lambda: tiny.fill_(0), lambda: tiny.fill_(1))
+    out = {"report": "fixed_cost", "device": torch.cuda.get_device_name(dev),
+           "l2": "evicted before every call", "floor_us": min(floor),
+           "ctypes_call_us": host_us(lambda: L.raw.adaln_strerror(0)), "cases": []}
+    from adaln_video_dit_gb300 import inputs as I
+    for name in ("wan13b", "mmdit_joint", "long_video", "shape_1x1024x5120"):
+        if name.startswith("shape"):
+            c = I.random_case(11, 1024, 5120, 1, dtype="bf16")
+            c["name"] = name
+        else:
+            c = host_inputs(name)
+        T, D, nseg = c["T"], c["D"], c["nseg"]
+        d = {k: torch_view(c[k]).to(dev) for k in ("x", "dy", "shift", "scale", "seg_id")}
+        y, dx = torch.empty_like(d["x"]), torch.empty_like(d["x"])
+        mean, rstd = torch.empty(T, device=dev), torch.empty(T, device=dev)
+        dsh, dsc = torch.empty(nseg, D, device=dev), torch.empty(nseg, D, device=dev)
+        nws = L.adaln_bwd_workspace_size(T, D, nseg, torch.bfloat16)
+        ws = torch.empty(nws, device=dev, dtype=torch.uint8)
+        fa = (P(d["x"]), P(d["shift"]), P(d["scale"]), P(d["seg_id"]), T, D, nseg, L.ADALN_BF16,
+              ctypes.c_float(1e-6), P(y), P(mean), P(rstd), S)
+        ba = (P(d["dy"]), P(d["x"]), P(mean), P(rstd), P(d["scale"]), P(d["seg_id"]), T, D, nseg,
+              L.ADALN_BF16, P(dx), P(dsh), P(dsc), P(ws), ctypes.c_size_t(nws), S)
+
+        def fwd_py():
+            L.adaln_fwd(d["x"], d["shift"], d["scale"], d["seg_id"], 1e-6, y=y, mean=mean,
+                        rstd=rstd, stream=st)
+
+        def bwd_py():
+            L.adaln_bwd(d["dy"], d["x"], mean, rstd, d["scale"], d["seg_id"], dx=dx, dshift=dsh,
+                        dscale=dsc, workspace=ws, stream=st)
+
+        fwd_raw = lambda: L.raw.adaln_fwd(*fa)  # noqa: E731
+        bwd_raw = lambda: L.raw.adaln_bwd(*ba)  # noqa: E731
+        for _ in range(3):
+            fwd_raw()
+            bwd_raw()
+        torch.cuda.synchronize(dev)
+        g_f, g_b = gpu_us(fwd_raw, bwd_raw)
+        L.adaln_trace_begin(3 * K + 8)
+        gpu_us(fwd_raw, bwd_raw)
+        L.adaln_trace_end()
+        trace = {nm: 1e3 * L.adaln_trace_get(k)[1] / max(1, L.adaln_trace_get(k)[0])
+                 for k, nm in L.KERNEL_NAMES.items()}
+        ab = alg_bytes(T, D, nseg, 2)
+        peak, kind = peaks()
+        out["cases"].append({
+            "workload": c["name"], "T": T, "D": D, "nseg": nseg,
+            "host_us": {"fwd_raw": host_us(fwd_raw), "bwd_raw": host_us(bwd_raw),
+                        "fwd_binding": host_us(fwd_py), "bwd_binding": host_us(bwd_py)},
+            "gpu_us": {"fwd": g_f, "bwd": g_b},
+            "trace_us": trace,
+            "at_peak_us": {"fwd": ab["fwd"] / (peak * 1e3), "bwd": ab["bwd"] / (peak * 1e3)},
+            "peak_gbs": peak, "peak_kind": kind})
+        rc, bits = L.adaln_get_status()
+        if rc != L.ADALN_OK:
+            raise RuntimeError(f"device status: {L.strerror(rc)} ({bits})")
+        del d, y, dx, ws
+        torch.cuda.empty_cache()
+    print(json.dumps(out), flush=True)
+
+
 def report_unfused(args):
     import torch
     import torch.nn.functional as F
@@ -872,6 +983,9 @@ def main():
         return
     if args.report == "shapes":
         report_shapes(args)
+        return
+    if args.report == "fixed-cost":
+        report_fixed_cost(args)
         return
     rank, local, world, pg = dist_setup(args.gpus)
     if args.sites > 1 and args.impl == "native":
