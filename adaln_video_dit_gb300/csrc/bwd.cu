@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
       for (int r = 0; r < R; ++r) {
         part[r][0] = part[r][1] = 0.0f;
         if (ok && r >= lo && r < hi) {
-          const float2 nm = splat2(-cmu[r]), r2 = splat2(crs[r]);
+          // xhat = x rstd - mean rstd: one FMA per element.
+          const float2 r2 = splat2(crs[r]), nmr = splat2(-cmu[r] * crs[r]);
           float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
           for (int q = 0; q < VPT; ++q) {
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
               E::unpack2(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
 #pragma unroll
               for (int e = 0; e < H; ++e) {
-                const float2 xh = mul2(add2(fx[e], nm), r2);
+                const float2 xh = fma2(fx[e], r2, nmr);
                 const float2 g = mul2(fd[e], s1[q][e]);
                 p0 = add2(p0, g);
                 p1 = fma2(g, xh, p1);
@@ -253,15 +254,17 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
       phase ^= 1;
 
       // Phase 2: dx = rstd (g - mean g - xhat mean(g xhat)), rearranged as
-      //   dx = dy (rstd (1 + scale)) + (x - mean) k1 + k0,
-      //   k1 = -rstd^2 mean(g xhat),  k0 = -rstd mean(g).
+      //   dx = dy (rstd (1 + scale)) + x k1 + (k0 - mean k1),
+      //   k1 = -rstd^2 mean(g xhat),  k0 = -rstd mean(g)
+      // (three packed operations per pair of elements).
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         if (r >= lo && r < hi) {
           const int64_t t = r0 + k * R + r;
-          const float2 nm = splat2(-cmu[r]), r2 = splat2(crs[r]);
-          const float2 k0 = splat2(-crs[r] * (part[r][0] * a.inv_d));
-          const float2 k1 = splat2(-(crs[r] * crs[r]) * (part[r][1] * a.inv_d));
+          const float2 r2 = splat2(crs[r]);
+          const float k1s = -(crs[r] * crs[r]) * (part[r][1] * a.inv_d);
+          const float2 k1 = splat2(k1s);
+          const float2 k0 = splat2(fmaf(-cmu[r], k1s, -crs[r] * (part[r][0] * a.inv_d)));
 #pragma unroll
           for (int q = 0; q < VPT; ++q) {
             if (valid[q]) {
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
               E::unpack2(ld_shared_v4(st0 + (uint32_t)((R + r) * nvec + v) * 16), fd);
 #pragma unroll
               for (int e = 0; e < H; ++e)
-                fx[e] = fma2(fd[e], mul2(s1[q][e], r2), fma2(add2(fx[e], nm), k1, k0));
+                fx[e] = fma2(fd[e], mul2(s1[q][e], r2), fma2(fx[e], k1, k0));
               st_global_cs_v4(static_cast<unsigned char*>(a.dx) + ((size_t)t * nvec + v) * 16,
                               E::pack2(fx));
             }
