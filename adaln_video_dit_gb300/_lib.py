@@ -25,7 +25,7 @@ KERNEL_NAMES = {0: "adaln_fwd_kernel", 1: "adaln_bwd_rows_kernel",
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 EXPORTS = ["adaln_fwd", "adaln_bwd_workspace_size", "adaln_bwd", "adaln_bwd_noalloc",
-           "adaln_get_status", "adaln_strerror", "adaln_trace_begin",
+           "adaln_get_status", "adaln_status_bind", "adaln_strerror", "adaln_trace_begin",
            "adaln_trace_end", "adaln_trace_get", "adaln_launch_shape",
            "adaln_selftest_wait_timeout", "adaln_fwd_bwd_host_scratch_size",
            "adaln_fwd_bwd_host"]
@@ -56,6 +56,8 @@ def _load():
     lib.adaln_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, ci, vp, vp, vp, vp]
     lib.adaln_get_status.restype = ci
     lib.adaln_get_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.adaln_status_bind.restype = ci
+    lib.adaln_status_bind.argtypes = [vp]
     lib.adaln_strerror.restype = ctypes.c_char_p
     lib.adaln_strerror.argtypes = [ci]
     lib.adaln_trace_begin.restype = ci
@@ -267,6 +269,14 @@ def adaln_get_status(stream=None, device=None):
     dev = device if device is not None else torch.cuda.current_device()
     rc = raw.adaln_get_status(ctypes.byref(bits), _stream_ptr(stream, dev))
     return rc, bits.value
+
+
+def adaln_status_bind(word):
+    """Bind a caller-owned device status word (an int32 CUDA tensor of one
+    element, zeroed) for the calls this host thread makes; None unbinds."""
+    if word is not None:
+        _dev(word, "status word", torch.int32, (1,))
+    _check(raw.adaln_status_bind(_ptr(word)), "adaln_status_bind")
 
 
 def adaln_strerror(code):

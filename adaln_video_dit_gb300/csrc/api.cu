@@ -82,7 +82,14 @@ cudaError_t get_shape(int which, int64_t T, int32_t D, adaln_dtype_t dt, Shape* 
 std::mutex g_status_mu;
 unsigned* g_status_ptr[kMaxDevices] = {};
 
+// Status word bound by the calling host thread (adaln_status_bind), or none.
+thread_local unsigned* t_bound_status = nullptr;
+
 cudaError_t status_ptr(unsigned** out) {
+  if (t_bound_status != nullptr) {
+    *out = t_bound_status;
+    return cudaSuccess;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -321,6 +328,12 @@ int adaln_get_status(uint32_t* host_bits, void* stream) {
   if (host_bits) *host_bits = bits;
   if (bits & (ADALN_DEV_SEG_RANGE | ADALN_DEV_SEG_ORDER)) return ADALN_ERR_SEG;
   if (bits & ADALN_DEV_TIMEOUT) return ADALN_ERR_TIMEOUT;
+  return ADALN_OK;
+}
+
+int adaln_status_bind(uint32_t* device_word) {
+  if (device_word != nullptr && !aligned(device_word, 4)) return ADALN_ERR_ALIGN;
+  t_bound_status = reinterpret_cast<unsigned*>(device_word);
   return ADALN_OK;
 }
 

@@ -479,17 +479,20 @@ def run_e2e(args, c, h, dev, stream, L, tdt, pg, clocks):
     K = args.e2e_steps
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     with clocks.window("e2e"):
-        e0.record(stream)
-        for _ in range(K):
+        ev[0].record(stream)
+        for i in range(K):
             step()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-    ms = max_over_ranks(pg, e0.elapsed_time(e1) / K, dev)
+    ms = max_over_ranks(pg, ev[0].elapsed_time(ev[K]) / K, dev)
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
     bi = sum(v.numel() * v.element_size() for v in hin.values())
     bo = sum(v.numel() * v.element_size() for v in hout.values())
-    return dict(ms_per_step=ms, h2d=bi, d2h=bo, steps=K, link=link)
+    return dict(ms_per_step=ms, h2d=bi, d2h=bo, steps=K, link=link,
+                step_ms={"median": statistics.median(per_step), "min": min(per_step),
+                         "max": max(per_step)})
 
 
 # ---------------------------------------------------------------------------
@@ -1039,6 +1042,7 @@ def main():
                 "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
                 "api": "adaln_fwd_bwd_host",
                 "host_link_gbs": e2e["link"],
+                "step_ms_spread": e2e["step_ms"],
                 "link_bound_ms": 1e3 * max(e2e["h2d"] / (e2e["link"]["h2d_gbs"] * 1e9),
                                            e2e["d2h"] / (e2e["link"]["d2h_gbs"] * 1e9))},
         }

@@ -36,8 +36,9 @@
  * report errors detectable on the host before launch, and launch failures.
  * Data errors found on the device (a seg_id outside [0, nseg) or decreasing
  * along the rows) are clamped so that every access stays in bounds, and are
- * recorded in a per-device status word read by adaln_get_status(); outputs of
- * such a call are unspecified.
+ * recorded in a status word read by adaln_get_status() (per device, or one the
+ * calling thread bound with adaln_status_bind()); outputs of such a call are
+ * unspecified.
  *
  * Preconditions (checked, ADALN_ERR_* on violation):
  *   - T >= 0 (T = 0 does nothing, except that adaln_bwd zeroes dshift/dscale);
@@ -203,12 +204,28 @@ ADALN_API int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shif
               int64_t chunk_rows, void* scratch, size_t scratch_bytes, void* stream);
 
 /*
- * Synchronise `stream`, then read and clear the current device's status word.
+ * Synchronise `stream`, then read and clear the status word: the one the
+ * calling thread bound (adaln_status_bind), else the current device's.
  * *host_bits (if non-NULL) receives the ADALN_DEV_* bits.  Returns ADALN_OK,
- * ADALN_ERR_SEG, ADALN_ERR_TIMEOUT or ADALN_ERR_CUDA.  The word is shared by
- * all calls on the device since it was last cleared.
+ * ADALN_ERR_SEG, ADALN_ERR_TIMEOUT or ADALN_ERR_CUDA.  The device's word is
+ * shared by all calls on the device that use it since it was last cleared.
  */
 ADALN_API int adaln_get_status(uint32_t* host_bits, void* stream);
+
+/*
+ * Bind a caller-owned device status word for the calls the calling host
+ * thread makes from now on (its kernels OR ADALN_DEV_* bits into it, and
+ * adaln_get_status() reads and clears it), instead of the device's shared
+ * word; NULL returns to the shared word.  For callers that drive several
+ * streams: with one word per stream (bound by the thread issuing that
+ * stream's calls), a data error is reported to the caller whose call caused
+ * it.  `device_word` is a 4-byte aligned uint32 in device memory of the
+ * device the calls run on, owned by the caller, zeroed by the caller before
+ * first use, and left bound until unbound or the thread exits (the library
+ * keeps only the pointer).  Returns ADALN_OK or ADALN_ERR_ALIGN.  The paper
+ * describes no status reporting; this is the library's own.
+ */
+ADALN_API int adaln_status_bind(uint32_t* device_word);
 
 /* Static description of a status code. */
 ADALN_API const char* adaln_strerror(int code);

@@ -112,6 +112,11 @@ def test_trace_argument_checks(lib):
     assert n.value == 0 and ms.value == 0.0
 
 
+def test_status_bind_checks_alignment_on_host(lib):
+    assert lib.raw.adaln_status_bind(ctypes.c_void_p(0x1002)) == lib.ADALN_ERR_ALIGN
+    assert lib.raw.adaln_status_bind(None) == lib.ADALN_OK  # unbinding needs no GPU
+
+
 def test_selftest_limit_is_checked_on_host(lib):
     assert lib.raw.adaln_selftest_wait_timeout(0, None) == lib.ADALN_ERR_ARG
     assert lib.raw.adaln_selftest_wait_timeout(100001, None) == lib.ADALN_ERR_ARG

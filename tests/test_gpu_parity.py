@@ -281,3 +281,41 @@ def test_cuda_graph_capture_matches_eager(adaln):
     for k in ref:
         assert torch.equal(out[k], ref[k]), k
 
+
+
+def test_bound_status_words_keep_callers_apart(adaln):
+    """Two host threads, each with its own bound status word: the thread
+    whose call has a decreasing seg_id sees the order bit, the other thread
+    and the device's shared word see nothing."""
+    import threading
+    dev = "cuda"
+    T, D, nseg = 600, 256, 4
+    x = torch.randn(T, D, device=dev).to(torch.bfloat16)
+    sh = torch.randn(nseg, D, device=dev).to(torch.bfloat16)
+    good = torch.from_numpy(np.repeat(np.arange(nseg), T // nseg).astype(np.int32)).to(dev)
+    bad = torch.from_numpy(np.r_[np.ones(300) * 2, np.zeros(300)].astype(np.int32)).to(dev)
+    words = {k: torch.zeros(1, device=dev, dtype=torch.int32) for k in ("good", "bad")}
+    results = {}
+
+    def worker(name, seg):
+        s = torch.cuda.Stream()
+        adaln.adaln_status_bind(words[name])
+        try:
+            with torch.cuda.stream(s):
+                y, m, r = adaln.adaln_fwd(x, sh, sh, seg, 1e-6, stream=s)
+                adaln.adaln_bwd(x, x, m, r, sh, seg, stream=s)
+            results[name] = adaln.adaln_get_status(stream=s)
+        finally:
+            adaln.adaln_status_bind(None)
+
+    threads = [threading.Thread(target=worker, args=(n, sg)) for n, sg in (("good", good),
+                                                                          ("bad", bad))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert results["good"] == (adaln.ADALN_OK, 0)
+    rc, bits = results["bad"]
+    assert rc == adaln.ADALN_ERR_SEG and bits & adaln.ADALN_DEV_SEG_ORDER
+    assert adaln.adaln_get_status() == (adaln.ADALN_OK, 0)  # the shared word stayed clean
+    assert int(words["good"].item()) == 0 and int(words["bad"].item()) == 0  # read and cleared
