@@ -57,9 +57,11 @@ ADALN_HD constexpr int variant_min_blocks(int v) {
   return v == 3 ? 1 : ((v == 4 || v == 6) ? 3 : (v == 5 ? 4 : 2));
 }
 ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v) + 1) * 32; }
-// Rows per reduction round.  A round's latency hardly depends on the row
-// length, so short rows take more rows per round (as registers allow).
-ADALN_HD constexpr int fwd_rows(int v) { return v == 5 ? 8 : 4; }
+// Rows per reduction round (and per ring stage).  The forward takes 4 in
+// every variant: for short rows 8 made a round long and split a CTA's rows
+// unevenly over its 4 teams (wan13b forward 20.9 vs 18.4 us).  The backward
+// takes 4 for short rows, 2 otherwise (two tensors per stage).
+ADALN_HD constexpr int fwd_rows(int v) { return (void)v, 4; }
 ADALN_HD constexpr int bwd_rows(int v) { return v == 6 ? 4 : 2; }
 // The row fills the variant's largest consumer-warp count exactly.
 ADALN_HD inline bool variant_exact(int v, int nvec) {
