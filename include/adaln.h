@@ -123,9 +123,10 @@ ADALN_API int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg,
  * are unspecified and may differ between runs: teams whose clamped segment
  * paths cross can share a partial slot.)  `workspace` (at least
  * adaln_bwd_workspace_size bytes, 16-byte aligned) is scratch owned by the
- * caller; its contents on entry do not matter.  Calls sharing one workspace must not overlap on the device.
- * A NULL workspace is ADALN_ERR_NULL (adaln_bwd_noalloc serves callers
- * without one); a short one is ADALN_ERR_WORKSPACE.
+ * caller; its contents on entry do not matter.  Calls sharing one workspace
+ * must not overlap on the device.  A NULL workspace is ADALN_ERR_NULL
+ * (adaln_bwd_noalloc serves callers without one); a short one is
+ * ADALN_ERR_WORKSPACE.
  */
 ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
               const float* rstd, const void* scale, const int32_t* seg_id,
@@ -146,9 +147,9 @@ ADALN_API int adaln_bwd(const void* dy, const void* x, const float* mean,
  * exits.  The partials grow with the SM count (G = SMs x teams per SM):
  * 3072-wide bf16 rows with 822 segments fit up to 181 SMs.  Sizes whose
  * adaln_bwd_workspace_size exceeds it are rejected with ADALN_ERR_WORKSPACE
- * before anything is launched.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls on a device share the array and it
+ * before anything is launched.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls on a device share the array and it
  * keeps the last call's contents (nothing in it needs to start at zero);
  * calls that overlap on the GPU race on it.  No cudaMalloc, cudaFree or other
  * allocating routine is called.
@@ -190,8 +191,8 @@ ADALN_API int adaln_bwd_noalloc(const void* dy, const void* x, const float* mean
  * Errors: ADALN_ERR_DIM, _DTYPE as for adaln_fwd; ADALN_ERR_NULL for a NULL
  * pointer (row pointers may be NULL when T = 0); ADALN_ERR_ARG for a bad eps
  * or a negative chunk_rows; ADALN_ERR_ALIGN when scratch is not 256-byte
- * aligned; ADALN_ERR_WORKSPACE when
- * scratch_bytes is too small; ADALN_ERR_CUDA when a copy or launch fails
+ * aligned; ADALN_ERR_WORKSPACE when scratch_bytes is too small;
+ * ADALN_ERR_CUDA when a copy or launch fails
  * (work enqueued before the failure may still run).  Device data errors go
  * to the status word as for the device calls.
  */
