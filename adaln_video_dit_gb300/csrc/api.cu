@@ -110,7 +110,6 @@ struct SlotPool {
   cudaEvent_t ev[kLaunchSlots] = {};
   bool recorded[kLaunchSlots] = {};
   bool pending[kLaunchSlots] = {};  // handed out, event not yet recorded
-  unsigned gen[kLaunchSlots] = {};
   int cursor = 0;
 };
 std::mutex g_slot_mu;
@@ -158,7 +157,7 @@ int cuda_fail(cudaError_t e) {
 
 namespace adaln {
 
-int launch_slot_acquire(int pool, cudaStream_t st, unsigned* generation) {
+int launch_slot_acquire(int pool, cudaStream_t st) {
   if (pool < 0 || pool >= kNumSlotPools) return -1;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
@@ -182,8 +181,6 @@ int launch_slot_acquire(int pool, cudaStream_t st, unsigned* generation) {
     }
     p.pending[slot] = true;
     p.cursor = (slot + 1) % kLaunchSlots;
-    if (++p.gen[slot] == 0) p.gen[slot] = 1;
-    if (generation) *generation = p.gen[slot];
     return slot;
   }
   return -1;

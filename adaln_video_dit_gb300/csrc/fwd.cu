@@ -408,7 +408,7 @@ cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
   int slot = -1;
   if (want_device_units(a, s, fwd_rows(s.variant))) {
     int* base = fwd_tickets_base();
-    if (base) slot = launch_slot_acquire(kPoolFwdUnits, st, nullptr);
+    if (base) slot = launch_slot_acquire(kPoolFwdUnits, st);
     if (slot >= 0) args.ticket = base + 2 * slot;
   }
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};

@@ -169,12 +169,11 @@ int check_dims_public(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dt);
 // indexes a static device array with it.  A slot is handed out only when the
 // launch that used it before has completed (a CUDA event per slot), so no two
 // launches in flight share one; launches being captured into a CUDA graph get
-// none (a graph may be replayed while other work runs).  Each acquisition
-// also returns the slot's generation, counting its uses from 1.
+// none (a graph may be replayed while other work runs).
 constexpr int kLaunchSlots = 256;
 enum { kPoolFwdUnits = 0, kNumSlotPools = 1 };
 // A slot index, or -1 when none is free (or the stream is capturing).
-int launch_slot_acquire(int pool, cudaStream_t st, unsigned* generation);
+int launch_slot_acquire(int pool, cudaStream_t st);
 // After the launch: the slot stays busy until the work queued on `st` ends.
 cudaError_t launch_slot_release(int pool, int slot, cudaStream_t st, bool launched);
 
