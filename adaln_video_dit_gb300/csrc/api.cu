@@ -212,7 +212,8 @@ int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* 
   unsigned* status = nullptr;
   e = status_ptr(&status);
   if (e != cudaSuccess) return cuda_fail(e);
-  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, 1.0f / (float)D, status};
+  FwdArgs a{x, shift, scale, seg_id, y, mean, rstd, T, D, nseg, eps, 1.0f / (float)D, status,
+            nullptr, 0};
   e = traced(ADALN_KERNEL_FWD, st, [&] { return launch_fwd(a, dtype, s, st); });
   return e == cudaSuccess ? ADALN_OK : cuda_fail(e);
 }

@@ -26,8 +26,10 @@ namespace adaln {
 // CTAs split the rows into contiguous ranges and the teams of a CTA share
 // its range through a shared-memory counter (then a segment's modulation
 // rows are loaded once per team, not once per unit: the mode for many short
-// segments, and for launches captured into CUDA graphs).  Every row's result
-// is independent of which team computes it.
+// segments, and for launches captured into CUDA graphs).  In between, the
+// CTAs share the first rows in contiguous ranges and all teams share a
+// device-wide tail (a.tail_rows).  Every row's result is independent of
+// which team computes it.
 // EXACT: the row fills the variant's largest consumer-warp count exactly
 // (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
 // the warp count and row length are compile-time constants (offsets fold
@@ -59,12 +61,23 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
 
   if (warp == nc) {  // producer warp
     if ((lt & 31) == 0) {
+      const unsigned char* src[1] = {static_cast<const unsigned char*>(a.x)};
       if (a.ticket != nullptr) {
-        // All rows, units claimed device-wide.  The last producer to finish
-        // (every claim of every producer is done by then) zeroes the
-        // counter pair for the next launch that is given it.
-        const unsigned char* src[1] = {static_cast<const unsigned char*>(a.x)};
-        ring_produce_units<R, 1>(rg, src, 0, a.T, R, row_bytes, a.ticket, a.seg, a.status);
+        if (a.tail_rows > 0) {
+          // The CTA's share of the first T - tail rows through the CTA's
+          // counter, then the last tail rows device-wide.
+          const int64_t TL = a.T - a.tail_rows;
+          const int64_t l0 = part_begin(blockIdx.x, TL, G);
+          ring_produce_units<R, 1>(rg, src, l0, part_begin(blockIdx.x + 1, TL, G) - l0,
+                                   next_unit, TL, a.tail_rows, a.ticket, R, row_bytes, a.seg,
+                                   a.status);
+        } else {
+          // All rows, units claimed device-wide.
+          ring_produce_units<R, 1>(rg, src, 0, 0, nullptr, 0, a.T, a.ticket, R, row_bytes,
+                                   a.seg, a.status);
+        }
+        // The last producer to finish (every claim of every producer is done
+        // by then) zeroes the counter pair for the next launch given it.
         __threadfence();
         const int producers = (int)gridDim.x * (int)(blockDim.x / team_threads);
         if (atomicAdd(a.ticket + 1, 1) == producers - 1) {
@@ -73,9 +86,8 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
           a.ticket[1] = 0;
         }
       } else {
-        const unsigned char* src[1] = {
-            static_cast<const unsigned char*>(a.x) + (size_t)r0 * row_bytes};
-        ring_produce_units<R, 1>(rg, src, r0, nrows, R, row_bytes, next_unit, a.seg, a.status);
+        ring_produce_units<R, 1>(rg, src, r0, nrows, next_unit, 0, 0, nullptr, R, row_bytes,
+                                 a.seg, a.status);
       }
     }
     return;
@@ -382,22 +394,37 @@ int* fwd_tickets_base() {
   return base[dev];
 }
 
-// Device-wide units pay when a team's consecutive units rarely change
-// segment (a segment's modulation rows are reloaded at each change): when
-// segments are at least 4 rounds of all teams long.
-bool want_device_units(const FwdArgs& a, const Shape& s, int R) {
+// How the forward's teams get their rows.  Device-wide units balance the
+// SMs' unequal speeds but make a team's consecutive units often change
+// segment, which reloads the segment's modulation rows: all rows go
+// device-wide when segments are at least 4 rounds of all teams long.
+// Otherwise each CTA's teams share the CTA's contiguous range, and, when
+// there are at least 10 rounds of rows and segments of at least one round,
+// the last tenth of the rows is shared device-wide, so that teams on faster
+// SMs take the tail (a reload at each of those few units): mmdit_joint's
+// forward 80.2 vs 78.0 us; with fewer rows the tail is too large a share
+// (wan13b +0.5 us), with shorter segments the reloads cost more than the
+// balance gains (mixed_varlen +0.2 %).  Returns the rows of that device-wide
+// tail, 0 for all rows device-wide, -1 for CTA ranges only.
+int64_t device_rows_plan(const FwdArgs& a, const Shape& s, int R) {
+  const int64_t round_rows = (int64_t)s.grid * s.teams * R;
+  int mode = 0;
+  if (a.T >= 2 * round_rows && a.T / a.nseg >= 4 * round_rows) mode = 1;
+  else if (a.T >= 10 * round_rows && a.T / a.nseg >= round_rows) mode = 2;
 #ifdef ADALN_TUNING
-  // Tuning builds only: ADALN_FWD_SCHED = "cta" or "device" forces a mode.
+  // Tuning builds only: ADALN_FWD_SCHED = "cta", "device" or "hybrid".
   if (const char* env = getenv("ADALN_FWD_SCHED")) {
-    if (env[0] == 'c') return false;
-    if (env[0] == 'd') return true;
+    if (env[0] == 'c') mode = 0;
+    if (env[0] == 'd') mode = 1;
+    if (env[0] == 'h') mode = 2;
   }
 #endif
-  const int64_t round_rows = (int64_t)s.grid * s.teams * R;
-  return a.T >= 2 * round_rows && a.T / a.nseg >= 4 * round_rows;
-}
-
-}  // namespace
+  if (mode == 0 || a.T < 2 * round_rows) return -1;
+  if (mode == 1) return 0;
+  int64_t tail = a.T / 10 / R * R;
+  if (tail < round_rows) tail = round_rows;
+  return tail < a.T / 2 ? tail : -1;
+}}  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st) {
@@ -405,11 +432,16 @@ cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
   int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   FwdArgs args = a;
   args.ticket = nullptr;
+  args.tail_rows = 0;
   int slot = -1;
-  if (want_device_units(a, s, fwd_rows(s.variant))) {
+  const int64_t plan = device_rows_plan(a, s, fwd_rows(s.variant));
+  if (plan >= 0) {
     int* base = fwd_tickets_base();
     if (base) slot = launch_slot_acquire(kPoolFwdUnits, st);
-    if (slot >= 0) args.ticket = base + 2 * slot;
+    if (slot >= 0) {
+      args.ticket = base + 2 * slot;
+      args.tail_rows = plan;
+    }
   }
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
   const cudaError_t e = cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);

@@ -101,6 +101,10 @@ struct FwdArgs {
   // Device-wide unit counter {next unit, producers done} of this launch, or
   // nullptr: the teams then share their CTA's contiguous row range only.
   int* ticket;
+  // With a ticket: 0 = all rows in device-wide units; > 0 = the CTAs share
+  // the first T - tail_rows rows in contiguous ranges and the last tail_rows
+  // go device-wide.
+  int64_t tail_rows;
 };
 
 struct BwdArgs {

@@ -122,30 +122,59 @@ __device__ __forceinline__ void ring_produce(const Ring& rg,
   }
 }
 
-// Producer loop of a team that claims its work (one lane).  Rows
-// [r0, r0 + nrows) are cut into units of U rows (a multiple of R) that the
-// teams take in turn from the counter *next_unit (in shared memory: the
-// teams of one CTA share the CTA's range; in global memory: all teams share
-// all rows), so a team that runs faster takes more and all finish together.
-// The next unit is claimed while the current one streams, hiding the
-// counter's latency.  A unit goes through the ring in stages of up to R rows;
-// each stage's meta (rows, raw segment id of the row before it or -1, first
-// row, segment ids of its rows) is written before the producer's arrival on
-// the stage's "full" barrier, which releases it with the data.  When no unit
-// is left the stage gets rows = -1 and no data.  Drains like ring_produce.
+// Producer loop of a team that claims its work (one lane).  Work comes from
+// up to two sources, taken in order: rows [l0, l0 + nl) cut into units of U
+// rows (a multiple of R) claimed from the counter *lctr, then rows
+// [g0, g0 + ng) in units claimed from *gctr (a null counter: no such
+// source).  A counter in shared memory lets the teams of one CTA share the
+// CTA's rows; one in global memory lets all teams share the rows, so a team
+// that runs faster takes more and all finish together.  The next unit is
+// claimed while the current one streams, hiding the counter's latency.  A
+// unit goes through the ring in stages of up to R rows; each stage's meta
+// (rows, raw segment id of the row before it or -1, first row, segment ids of
+// its rows) is written before the producer's arrival on the stage's "full"
+// barrier, which releases it with the data.  When no unit is left the stage
+// gets rows = -1 and no data.  `src` holds the tensors' base addresses (rows
+// are absolute).  Before returning it waits for the newest copy into every
+// stage, so that no copy into this CTA's shared memory is still in flight
+// when the CTA exits.
 template <int R, int NT>
 __device__ __forceinline__ void ring_produce_units(const Ring& rg,
                                                    const unsigned char* const (&src)[NT],
-                                                   int64_t r0, int64_t nrows, int U,
-                                                   int row_bytes, int* next_unit,
-                                                   const int32_t* seg, unsigned* status) {
+                                                   int64_t l0, int64_t nl, int* lctr,
+                                                   int64_t g0, int64_t ng, int* gctr, int U,
+                                                   int row_bytes, const int32_t* seg,
+                                                   unsigned* status) {
   const uint64_t policy = l2_evict_first_policy();
-  const int64_t nunits = (nrows + U - 1) / U;
   const int S = rg.stages;
   const uint32_t stage_bytes = (uint32_t)R * row_bytes * NT;
   int64_t issued = 0;
+  int source = lctr != nullptr ? 0 : 1;  // 0: first source, 1: second, 2: none left
+  // Claim the next unit: its rows [*a, *b), or false when both sources are done.
+  auto claim = [&](int64_t* a, int64_t* b) -> bool {
+    if (source == 0) {
+      const int64_t u = atomicAdd(lctr, 1);
+      if (u * U < nl) {
+        *a = l0 + u * U;
+        *b = min(*a + U, l0 + nl);
+        return true;
+      }
+      source = 1;
+    }
+    if (source == 1 && gctr != nullptr) {
+      const int64_t u = atomicAdd(gctr, 1);
+      if (u * U < ng) {
+        *a = g0 + u * U;
+        *b = min(*a + U, g0 + ng);
+        return true;
+      }
+    }
+    source = 2;
+    return false;
+  };
   int64_t cur = 0, cur_end = 0;  // rows of the current unit not yet staged
-  int next = atomicAdd(next_unit, 1);
+  int64_t na = 0, nb = 0;        // the unit claimed ahead
+  bool ahead = claim(&na, &nb);
   int s = 0;        // stage of claim k (k % S, advanced by increment)
   uint32_t it = 0;  // use of that stage (k / S), for the "empty" parity
   for (int64_t k = 0;; ++k, it += (s + 1 == S), s = (s + 1 == S ? 0 : s + 1)) {
@@ -157,15 +186,15 @@ __device__ __forceinline__ void ring_produce_units(const Ring& rg,
     if (*rg.abort) break;
     int* m = rg.meta + s * kMetaInts;
     if (cur == cur_end) {
-      if (next >= nunits) {
+      if (!ahead) {
         m[0] = -1;
         mbar_arrive(rg.full(s));
         issued = k + 1;
         break;
       }
-      cur = (int64_t)next * U;
-      cur_end = min(cur + U, nrows);
-      next = atomicAdd(next_unit, 1);
+      cur = na;
+      cur_end = nb;
+      ahead = claim(&na, &nb);
     }
     const int rows = (int)min((int64_t)R, cur_end - cur);
     const uint32_t bytes = (uint32_t)rows * row_bytes;
@@ -176,7 +205,7 @@ __device__ __forceinline__ void ring_produce_units(const Ring& rg,
       bulk_g2s(dst + (uint32_t)i * R * row_bytes, src[i] + (size_t)cur * row_bytes, bytes,
                rg.full(s), policy);
     // Segment ids load while the copies are in flight.
-    const int64_t t = r0 + cur;
+    const int64_t t = cur;
     int sg[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) sg[r] = r < rows ? __ldg(seg + t + r) : 0;

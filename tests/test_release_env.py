@@ -72,3 +72,43 @@ def test_release_library_ignores_tuning_variables(adaln):
     plain = _child({})
     knobs = _child(KNOBS)
     assert plain == knobs
+
+
+MODES_CHILD = r"""
+import ctypes, hashlib, json, sys
+sys.path.insert(0, %(root)r)
+import numpy as np, torch
+from adaln_video_dit_gb300 import build as B, inputs as I
+lib = ctypes.CDLL(B.build(tuning=True))
+vp = ctypes.c_void_p
+lib.adaln_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                          ctypes.c_int, ctypes.c_float, vp, vp, vp, vp]
+c = I.random_case(9, 20000, 3072, 7, dtype="bf16")
+bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+x, sh, sc = (bf(c[k]) for k in ("x", "shift", "scale"))
+seg = torch.from_numpy(c["seg_id"]).cuda()
+y = torch.empty_like(x); m = torch.empty(c["T"], device="cuda"); r = torch.empty_like(m)
+P = lambda t: vp(t.data_ptr())
+st = vp(torch.cuda.current_stream().cuda_stream)
+assert lib.adaln_fwd(P(x), P(sh), P(sc), P(seg), c["T"], c["D"], c["nseg"], 1,
+                     ctypes.c_float(c["eps"]), P(y), P(m), P(r), st) == 0
+torch.cuda.synchronize()
+print(json.dumps({k: hashlib.sha256(t.cpu().contiguous().view(torch.uint8).numpy().tobytes()).hexdigest()
+                  for k, t in (("y", y), ("mean", m), ("rstd", r))}))
+"""
+
+
+@pytest.mark.gpu
+def test_forward_claim_modes_give_the_same_bits(adaln):
+    """The forward's rows may be streamed by any team (CTA ranges, device-wide
+    units, or CTA ranges with a device-wide tail): every row's result is the
+    same bit for bit.  The tuning build forces each mode."""
+    outs = []
+    for mode in ("cta", "device", "hybrid"):
+        env = {k: v for k, v in os.environ.items() if k not in KNOBS}
+        env["ADALN_FWD_SCHED"] = mode
+        r = subprocess.run([sys.executable, "-c", MODES_CHILD % {"root": ROOT}], env=env,
+                           capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append(json.loads(r.stdout.strip().splitlines()[-1]))
+    assert outs[0] == outs[1] == outs[2]
