@@ -322,26 +322,65 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
 // are visible.
 constexpr int kFinalizeThreads = 256;
 
+// First rows of segments b and b + 1 in the sorted seg_id (lower bounds of b
+// and b + 1, T when absent), found by the whole block: each round probes 256
+// evenly spaced rows of the remaining range and counts those below the
+// target (__syncthreads_count), which narrows the range 256-fold, so T rows
+// take ceil(log256 T) + 1 rounds of one load each.  On unsorted (invalid)
+// input the results are some rows in [0, T].
+__device__ __forceinline__ void segment_rows(const int32_t* seg, int64_t T, int b,
+                                             int64_t& sb, int64_t& eb) {
+  int64_t lo[2] = {0, 0}, hi[2] = {T, T};
+  while (hi[0] > lo[0] || hi[1] > lo[1]) {
+    int n[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t step = (hi[k] - lo[k] + kFinalizeThreads - 1) / kFinalizeThreads;
+      const int64_t p = lo[k] + threadIdx.x * step;
+      const bool below = hi[k] > lo[k] && p < hi[k] && __ldg(seg + p) < b + k;
+      n[k] = __syncthreads_count(below);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (hi[k] <= lo[k]) continue;
+      const int64_t step = (hi[k] - lo[k] + kFinalizeThreads - 1) / kFinalizeThreads;
+      if (n[k] == 0) {
+        hi[k] = lo[k];  // the first probe is not below: the bound is lo
+      } else {
+        // Probes 0 .. n-1 are below the target, probe n is not.
+        const int64_t top = lo[k] + n[k] * step;
+        lo[k] += (n[k] - 1) * step + 1;
+        if (top < hi[k]) hi[k] = top;
+      }
+    }
+  }
+  sb = lo[0];
+  eb = lo[1];
+}
+
 __global__ void __launch_bounds__(kFinalizeThreads, 4)
-    adaln_bwd_finalize_kernel(BwdArgs a, int G, int gpc) {
+    adaln_bwd_finalize_kernel(BwdArgs a, int G, int gpc, int search) {
   __shared__ float4 sh[kFinalizeThreads];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
   const int cb = kFinalizeThreads / gpc;   // columns per block
   const int ncol4 = a.D / 4;               // float4 columns of one half
   const int cl = threadIdx.x % cb, g = threadIdx.x / cb;
   const int col4 = blockIdx.y * cb + cl;   // in [0, 2 ncol4)
 
-  // Rows of segment b: [seg_start[b], seg_start[b + 1]), recorded by the
-  // row pass.  Clamped so that inconsistent input (reported in the status
-  // word) still reads inside the workspace.
+  // Rows of segment b, [sb, eb): with `search`, found in seg_id (an input)
+  // while the row pass still runs; else from the segment start table the
+  // row pass records.  Both agree on valid input.  Clamped so that
+  // inconsistent input (reported in the status word) still reads inside the
+  // workspace.
   int64_t sb = 0, eb = 0;
-  if (a.T > 0) {
+  if (search && a.T > 0) segment_rows(a.seg, a.T, b, sb, eb);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!search && a.T > 0) {
     sb = a.seg_start[b];
     eb = a.seg_start[b + 1];
-    sb = sb < 0 ? 0 : (sb > a.T ? a.T : sb);
-    eb = eb < 0 ? 0 : (eb > a.T ? a.T : eb);
   }
+  sb = sb < 0 ? 0 : (sb > a.T ? a.T : sb);
+  eb = eb < 0 ? 0 : (eb > a.T ? a.T : eb);
   float4 ps = make_float4(0.f, 0.f, 0.f, 0.f);
   if (eb > sb && col4 < 2 * ncol4) {
     const int64_t c0 = part_owner(sb, a.T, G), c1 = part_owner(eb - 1, a.T, G);
@@ -453,8 +492,12 @@ cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t s
   if (gpc > 1 && blocks(gpc) > 4 * (int64_t)s.sms && blocks(gpc / 2) <= 4 * (int64_t)s.sms)
     gpc /= 2;
   int G = (int)virtual_ctas(s);
+  // One wave of blocks starts while the row pass ends: they find their
+  // segment's rows in seg_id meanwhile.  With more blocks, the later ones
+  // start after the row pass and read the recorded table instead.
+  int search = blocks(gpc) <= 4 * (int64_t)s.sms ? 1 : 0;
   BwdArgs args = a;
-  void* params[] = {&args, &G, &gpc};
+  void* params[] = {&args, &G, &gpc, &search};
   cudaLaunchConfig_t cfg = {};
   const int cb = kFinalizeThreads / gpc;
   cfg.gridDim = dim3((unsigned)a.nseg, (unsigned)((2 * (a.D / 4) + cb - 1) / cb));
