@@ -628,9 +628,10 @@ def bench_config(c, world):
             "parallelism": f"replicas x{world} (no data-path collective)"}
 
 
-def load_traffic(kernel):
+def load_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/traffic.txt), if it was taken on the current kernel sources."""
+    (profiles/traffic.txt), if it was taken on this workload and on the
+    current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         vals = {}
@@ -641,6 +642,8 @@ def load_traffic(kernel):
                 k, v = line.split()
                 vals[k] = v
         from adaln_video_dit_gb300 import build as B
+        if vals.get("workload") != workload:
+            return None, "no ncu capture of this workload"
         if vals.get("source_hash") != B.source_hash():
             return None, "stale: kernels changed since the ncu capture"
         return int(vals[kernel]), "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"
@@ -1012,7 +1015,8 @@ def main():
         dom = "adaln_bwd_rows_kernel"
         dom_us = r["kernels"][dom]["avg_us"]
         achieved = ab["bwd_rows"] / (dom_us * 1e-6) / 1e9
-        traffic, traffic_note = load_traffic(dom)
+        traffic, traffic_note = load_traffic(
+            dom, args.workload if not args.rows else f"{args.workload}:{args.rows}")
         breakdown = {}
         for k, ms in (("fwd", r["fwd_ms"]), ("bwd", r["bwd_ms"]),
                       ("fwd_bwd", r["fwd_ms"] + r["bwd_ms"])):

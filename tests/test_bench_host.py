@@ -97,18 +97,22 @@ def test_nvml_sampler_reads_clocks_in_windows(monkeypatch):
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1234.0
 
 
-def test_traffic_lookup_follows_the_source_hash(tmp_path, monkeypatch):
+def test_traffic_lookup_follows_the_workload_and_source_hash(tmp_path, monkeypatch):
     os.makedirs(tmp_path / "profiles")
     p = tmp_path / "profiles" / "traffic.txt"
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    p.write_text(f"# comment\nsource_hash {B.source_hash()}\nadaln_bwd_rows_kernel 123\n")
-    assert bench.load_traffic("adaln_bwd_rows_kernel")[0] == 123
-    assert bench.load_traffic("adaln_fwd_kernel")[0] is None  # not captured
-    p.write_text("source_hash 0000000000000000\nadaln_bwd_rows_kernel 123\n")
-    v, note = bench.load_traffic("adaln_bwd_rows_kernel")
+    p.write_text(f"# comment\nworkload long_video\nsource_hash {B.source_hash()}\n"
+                 "adaln_bwd_rows_kernel 123\n")
+    assert bench.load_traffic("adaln_bwd_rows_kernel", "long_video")[0] == 123
+    assert bench.load_traffic("adaln_fwd_kernel", "long_video")[0] is None  # not captured
+    v, note = bench.load_traffic("adaln_bwd_rows_kernel", "wan13b")  # another workload
+    assert v is None and note == "no ncu capture of this workload"
+    assert bench.load_traffic("adaln_bwd_rows_kernel", "long_video:4096")[0] is None  # truncated
+    p.write_text("workload long_video\nsource_hash 0000000000000000\nadaln_bwd_rows_kernel 123\n")
+    v, note = bench.load_traffic("adaln_bwd_rows_kernel", "long_video")
     assert v is None and note.startswith("stale")
     p.unlink()
-    assert bench.load_traffic("adaln_bwd_rows_kernel") == (None, "no ncu capture")
+    assert bench.load_traffic("adaln_bwd_rows_kernel", "long_video") == (None, "no ncu capture")
 
 
 def test_source_hash_ignores_comments_only():
