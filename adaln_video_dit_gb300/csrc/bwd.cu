@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   const Ring rg = ring_layout(smem + team * team_bytes, stages, 1 + team, team * (nc + 1));
   if (lt == 0) ring_init_team(rg, nc);
   __syncthreads();
+  // Launched as a programmatic dependent of the stream's previous kernel
+  // (typically the forward that wrote mean and rstd): nothing in global
+  // memory is read before that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int64_t G = (int64_t)gridDim.x * teams;  // virtual CTAs
   const int64_t v = (int64_t)blockIdx.x * teams + team;
@@ -472,7 +476,7 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
   int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   BwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
-  return cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
+  return launch_dependent(k, s, params, st);
 }
 
 cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s, cudaStream_t st) {

@@ -52,6 +52,12 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   if (lt == 0) ring_init_team(rg, nc);
   if (threadIdx.x == 0) *next_unit = 0;
   __syncthreads();
+  // Launched as a programmatic dependent of the stream's previous kernel: the
+  // set-up above may overlap that kernel's end, nothing in global memory is
+  // read before it has completed.  The next kernel may then be scheduled as
+  // SMs free up (this library's kernels wait the same way before reading).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int64_t G = gridDim.x;
   const int64_t r0 = part_begin(blockIdx.x, a.T, G);
@@ -444,7 +450,7 @@ cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
     }
   }
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};
-  const cudaError_t e = cudaLaunchKernel(k, dim3(s.grid), dim3(s.threads), params, s.smem, st);
+  const cudaError_t e = launch_dependent(k, s, params, st);
   if (slot >= 0) {
     const cudaError_t r = launch_slot_release(kPoolFwdUnits, slot, st, e == cudaSuccess);
     if (e == cudaSuccess && r != cudaSuccess) return r;

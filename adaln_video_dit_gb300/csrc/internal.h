@@ -148,6 +148,24 @@ inline size_t bwd_workspace_bytes(const Shape& s, int32_t D, int32_t nseg) {
   return bwd_partials_bytes(s, D, nseg) + ((size_t)nseg + 1) * sizeof(int32_t);
 }
 
+// Launch a row kernel of shape s as a programmatic dependent of the previous
+// kernel on st (the kernel waits, griddepcontrol.wait, before reading global
+// memory).
+inline cudaError_t launch_dependent(void* kernel, const Shape& s, void** params,
+                                    cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)s.grid);
+  cfg.blockDim = dim3((unsigned)s.threads);
+  cfg.dynamicSmemBytes = (size_t)s.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kernel, params);
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st);
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt,
