@@ -379,6 +379,9 @@ __global__ void __launch_bounds__(kFinalizeThreads, 4)
   int64_t sb = 0, eb = 0;
   if (search && a.T > 0) segment_rows(a.seg, a.T, b, sb, eb);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The stream's next kernel (this library's row kernels wait before
+  // reading) may be scheduled as this grid's blocks finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!search && a.T > 0) {
     sb = a.seg_start[b];
     eb = a.seg_start[b + 1];

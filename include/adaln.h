@@ -32,7 +32,14 @@
  * never allocates, frees or retains caller memory.
  *
  * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
- * default stream) and the calls return without synchronising.  Return codes
+ * default stream) and the calls return without synchronising.  The kernels
+ * are launched as programmatic dependents of the stream's previous kernel:
+ * they may be scheduled while it ends, but read nothing before it has
+ * completed.  They also let the stream's next kernel be scheduled before they
+ * complete; a kernel launched after them with programmatic stream
+ * serialization must wait (cudaGridDependencySynchronize) before reading
+ * their outputs, as that launch mode requires anyway.  Ordinary launches,
+ * copies and events see the usual stream order.  Return codes
  * report errors detectable on the host before launch, and launch failures.
  * Data errors found on the device (a seg_id outside [0, nseg) or decreasing
  * along the rows) are clamped so that every access stays in bounds, and are
