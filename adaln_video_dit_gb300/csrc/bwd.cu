@@ -5,7 +5,7 @@
 // sequence by threads that each own a feature column d and accumulate down
 // the rows, so every warp access is contiguous along d.  Here that column
 // reduction is fused into the row pass: each persistent team (consumer warps
-// + a producer warp; a CTA per SM holds two or three) streams the contiguous
+// + a producer warp; a CTA per SM holds one to three) streams the contiguous
 // row range of its virtual CTA through a shared-memory ring (x and dy read
 // from HBM exactly once), computes dx per row (phase 1: the two row sums and
 // the column sums; phase 2: dx, both reading the rows from the stage), and
@@ -13,8 +13,9 @@
 // column.  At a segment change and at the end of its range a team writes one
 // fp32 partial per (virtual CTA, segment) to the workspace, and records the
 // first row of every segment it starts; a second launch (a programmatic
-// dependent) sums the partials of each segment in virtual-CTA order.  No
-// floating-point atomics, no inter-CTA waits.
+// dependent) sums the partials of each segment in virtual-CTA order, finding
+// the segment's rows in that table or, when its grid fits one wave, in seg_id
+// itself.  No floating-point atomics, no inter-CTA waits.
 //
 //   dx[t,d]      = rstd_t (g - mean_d g - xhat mean_d(g xhat)),  g = dy (1 + scale_b)
 //   dscale[b,d]  = sum over rows of segment b of dy xhat
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
 // The order of every sum is fixed by (T, G, nseg), so results are bitwise
 // reproducible.  Launched as a programmatic dependent of the row pass: it
 // waits (griddepcontrol.wait) until the row pass has completed and its writes
-// are visible.
+// are visible, reading only seg_id (an input) before that.
 constexpr int kFinalizeThreads = 256;
 
 // First rows of segments b and b + 1 in the sorted seg_id (lower bounds of b

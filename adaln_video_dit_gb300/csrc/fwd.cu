@@ -4,7 +4,7 @@
 // reduced on chip in two stages (warp shuffles, then across warps) and the
 // modulation is applied in the same launch, so x is read from HBM once and y
 // written once.  Here persistent teams (consumer warps + a producer warp,
-// two or three per CTA, one CTA per SM) claim units of R rows and stream them
+// one to four per CTA, one CTA per SM) claim units of R rows and stream them
 // through their shared-memory rings (bulk async copies issued by one producer
 // lane); for each round of R rows the consumer threads read their column
 // slice from the stage three times (row sums -> mean; centred sum of squares
