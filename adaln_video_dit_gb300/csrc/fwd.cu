@@ -274,6 +274,7 @@ void* fwd_kernel_for(int variant, bool exact) {
   switch (variant) {
     case 5: return fwd_kernel_for_v<E, 5>(exact);
     case 1: return fwd_kernel_for_v<E, 1>(exact);
+    case 4: return fwd_kernel_for_v<E, 4>(exact);
     case 2: return fwd_kernel_for_v<E, 2>(exact);
     default: return fwd_kernel_for_v<E, 3>(exact);
   }
@@ -301,6 +302,12 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   s->exact = variant_exact(variant, s->nvec);
   s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
+  // The kernel is compiled for `teams` teams of the variant's largest warp
+  // count; rows that need fewer consumer warps run more teams in the same
+  // thread (and register) budget, up to kMaxTeams, so that an SM keeps about
+  // as many warps, and rows, in flight.
+  const int fit = teams * variant_max_threads(variant) / ((s->nc + 1) * 32);
+  if (fit > teams) teams = fit < kMaxTeams ? fit : kMaxTeams;
   s->teams = teams;
   s->threads = teams * (s->nc + 1) * 32;
 
@@ -313,10 +320,10 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
     e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
 
-  // Ring depth: about 160 KB of staged rows per SM, split over the teams the
-  // variant is sized for, and no more than fits beside them.
-  const int units = variant_min_blocks(s->variant);  // teams per SM
-  const int ctas = units / teams < 1 ? 1 : units / teams;
+  // Ring depth: about 160 KB of staged rows per SM, split over the teams,
+  // and no more than fits beside them.
+  const int units = teams;  // teams per SM (one CTA per SM)
+  const int ctas = 1;
   const int stage_bytes = rows_per_round * s->row_bytes * ntensors;
   const int per_cta = smem_sm / ctas - 2048;  // room for the per-CTA reserve
   const int per_team = (per_cta - cta_header) / teams;

@@ -19,6 +19,8 @@ namespace adaln {
 constexpr int kRowsPerRound = 8;
 // Largest number of consumer warps in a team (any variant).
 constexpr int kMaxConsumerWarps = 8;
+// Most teams in one CTA (each uses named barrier 1 + its index).
+constexpr int kMaxTeams = 8;
 // Ints of stage meta per ring stage: rows in the stage (-1: no work left),
 // raw segment id of the row before it, first row (low, high 32 bits), then
 // kRowsPerRound segment ids.
@@ -38,13 +40,16 @@ constexpr int kCtaHeaderBytes = 128;
 // 16 allow 128.
 //   variant 5: nvec <=  192  VPT 2, <= 3 warps, 4 teams (forward)
 //   variant 6: nvec <=  192  VPT 2, <= 3 warps, 3 teams (backward)
-//   variant 1: nvec <=  384  VPT 2, <= 6 warps, 2 teams (forward)
+//   variant 1: nvec  =  384  VPT 2,    6 warps, 2 teams (forward)
 //   variant 4: nvec <=  384  VPT 4, <= 3 warps, 3 teams (backward: its column
-//              sums favour few warps per row, many rows per SM)
+//              sums favour few warps per row, many rows per SM; forward below
+//              384 vectors, where 2-warp teams fit four to an SM)
+// A row that needs fewer warps than the variant's largest count runs more,
+// smaller teams in the same thread budget (staging_shape).
 //   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 teams
 //   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 team
 ADALN_HD inline int choose_variant(int nvec) {
-  return nvec <= 192 ? 5 : (nvec <= 384 ? 1 : (nvec <= 640 ? 2 : 3));
+  return nvec <= 192 ? 5 : (nvec < 384 ? 4 : (nvec == 384 ? 1 : (nvec <= 640 ? 2 : 3)));
 }
 ADALN_HD inline int choose_bwd_variant(int nvec) {
   return nvec <= 192 ? 6 : (nvec <= 384 ? 4 : (nvec <= 640 ? 2 : 3));

@@ -65,8 +65,12 @@ EDGE = [
     (999, 24, 4, "f32", [1, 1, 1, 996]),   # one-row segments, nvec = 6
     (300, 1536, 2, "bf16", None),          # nvec 192: variants 5/6 (VPT 2), 3 warps
     (300, 1528, 2, "bf16", None),          # nvec 191: variants 5/6, ragged last vector
-    (300, 1544, 2, "bf16", None),          # nvec 193: variant 1 (VPT 2), 4 warps, ragged
-    (300, 3072, 3, "bf16", None),          # nvec 384: variant 1, 6 warps
+    (300, 1544, 2, "bf16", None),          # nvec 193: variant 4 (VPT 4), 2 warps, ragged
+    (600, 512, 3, "bf16", None),           # nvec 64: 1-warp teams, 8 forward / 6 backward
+    (600, 1024, 3, "bf16", None),          # nvec 128: 2-warp teams, 5 forward / 4 backward
+    (600, 2048, 3, "bf16", None),          # nvec 256: variant 4, 2-warp teams, 4 per CTA
+    (300, 3064, 3, "bf16", None),          # nvec 383: variant 4, 3 warps, ragged
+    (300, 3072, 3, "bf16", None),          # nvec 384: variant 1 forward, 6 warps
     (300, 3080, 3, "bf16", None),          # nvec 385: variant 2 (VPT 4), 4 warps, ragged
     (260, 5120, 3, "bf16", None),          # nvec 640: variant 2, 5 warps
     (260, 5128, 3, "bf16", None),          # nvec 641: variant 3 (VPT 4), 6 warps, ragged
@@ -245,6 +249,17 @@ def test_launch_shape_matches_the_rules(adaln):
     assert s["threads"] == 4 * 4 * 32 and s["grid"] == sms
     s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 5, 5120, 1, torch.bfloat16)
     assert s["grid"] == 5
+    # Rows that need fewer warps run more teams in the variant's thread
+    # budget: D = 1024 bf16 (128 vectors, 2 warps a team) gets five forward
+    # teams of 2 + 1 warps and four backward ones; D = 2048 bf16 (256
+    # vectors, 4 per thread) four teams of 2 + 1 warps both ways.
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 32768, 1024, 4, torch.bfloat16)
+    assert s["threads"] == 5 * 3 * 32
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_BWD_ROWS, 32768, 1024, 4, torch.bfloat16)
+    assert s["threads"] == 4 * 3 * 32
+    for which in (adaln.ADALN_KERNEL_FWD, adaln.ADALN_KERNEL_BWD_ROWS):
+        s = adaln.adaln_launch_shape(which, 32768, 2048, 4, torch.bfloat16)
+        assert s["threads"] == 4 * 3 * 32 and s["grid"] == sms
 
 
 def test_cuda_graph_capture_matches_eager(adaln):
