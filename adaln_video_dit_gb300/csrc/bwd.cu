@@ -83,13 +83,13 @@ __device__ __forceinline__ void flush_partials(float* partials, int64_t slot, in
 // ranges, partial slots and sums are those of teams x grid independent CTAs,
 // while the teams of one SM, being one CTA, get equal shares of it (two
 // separate CTAs on an SM run up to a tenth apart).
-template <class E, int VARIANT, int R, bool EXACT>
+template <class E, int VARIANT, int R, int NCX>
 __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_threads(VARIANT), 1)
     adaln_bwd_rows_kernel(BwdArgs a, int nc_rt, int stages, int nvec_rt, int team_bytes) {
   constexpr int VPT = variant_vpt(VARIANT);
-  constexpr int NC_X = variant_max_warps(VARIANT);
-  const int nc = EXACT ? NC_X : nc_rt;
-  const int nvec = EXACT ? NC_X * 32 * VPT : nvec_rt;
+  constexpr bool EXACT = NCX != 0;
+  const int nc = EXACT ? NCX : nc_rt;
+  const int nvec = EXACT ? NCX * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;
   extern __shared__ __align__(128) unsigned char smem[];
   // Let the finalize grid be scheduled as soon as SMs free up; it waits for
@@ -444,24 +444,29 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
 
 namespace {
 
-template <class E, int V>
-void* rows_kernel_for_v(bool exact) {
-  return exact ? reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, bwd_rows(V), true>)
-               : reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, bwd_rows(V), false>);
+template <class E, int V, int NCX>
+void* rows_inst() {
+  return reinterpret_cast<void*>(&adaln_bwd_rows_kernel<E, V, bwd_rows(V), NCX>);
 }
 
+// The instantiation for (variant, fixed warp count or 0); compiled_exact lists
+// the fixed counts.
 template <class E>
-void* rows_kernel_for(int variant, bool exact) {
+void* rows_kernel_for(int variant, int ncx) {
   switch (variant) {
-    case 6: return rows_kernel_for_v<E, 6>(exact);
-    case 2: return rows_kernel_for_v<E, 2>(exact);
-    case 4: return rows_kernel_for_v<E, 4>(exact);
-    default: return rows_kernel_for_v<E, 3>(exact);
+    case 6: return ncx == 1 ? rows_inst<E, 6, 1>() : ncx == 2 ? rows_inst<E, 6, 2>()
+                 : ncx == 3 ? rows_inst<E, 6, 3>() : rows_inst<E, 6, 0>();
+    case 4: return ncx == 2 ? rows_inst<E, 4, 2>() : ncx == 3 ? rows_inst<E, 4, 3>()
+                 : rows_inst<E, 4, 0>();
+    case 2: return ncx == 4 ? rows_inst<E, 2, 4>() : ncx == 5 ? rows_inst<E, 2, 5>()
+                 : rows_inst<E, 2, 0>();
+    default: return ncx == 6 ? rows_inst<E, 3, 6>() : ncx == 8 ? rows_inst<E, 3, 8>()
+                  : rows_inst<E, 3, 0>();
   }
 }
 
-void* pick_rows(adaln_dtype_t dt, int variant, bool exact) {
-  return dt == ADALN_BF16 ? rows_kernel_for<BF16>(variant, exact) : rows_kernel_for<F32>(variant, exact);
+void* pick_rows(adaln_dtype_t dt, int variant, int ncx) {
+  return dt == ADALN_BF16 ? rows_kernel_for<BF16>(variant, ncx) : rows_kernel_for<F32>(variant, ncx);
 }
 
 }  // namespace
@@ -470,13 +475,13 @@ cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_bwd_variant(nvec);
-  return staging_shape(pick_rows(dt, v, variant_exact(v, nvec)), T, D, dt, 2, bwd_rows(v), v,
+  return staging_shape(pick_rows(dt, v, exact_warps(v, nvec)), T, D, dt, 2, bwd_rows(v), v,
                        variant_min_blocks(v), 0, s);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, adaln_dtype_t dt, const Shape& s,
                             cudaStream_t st) {
-  void* k = pick_rows(dt, s.variant, s.exact);
+  void* k = pick_rows(dt, s.variant, s.ncx);
   int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   BwdArgs args = a;
   void* params[] = {&args, &nc, &stages, &nvec, &team_bytes};

@@ -34,13 +34,13 @@ namespace adaln {
 // (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
 // the warp count and row length are compile-time constants (offsets fold
 // into immediates, no per-vector guards).
-template <class E, int VARIANT, int R, bool EXACT>
+template <class E, int VARIANT, int R, int NCX>
 __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_threads(VARIANT), 1)
     adaln_fwd_kernel(FwdArgs a, int nc_rt, int stages, int nvec_rt, int team_bytes) {
   constexpr int VPT = variant_vpt(VARIANT);
-  constexpr int NC_X = variant_max_warps(VARIANT);
-  const int nc = EXACT ? NC_X : nc_rt;
-  const int nvec = EXACT ? NC_X * 32 * VPT : nvec_rt;
+  constexpr bool EXACT = NCX != 0;
+  const int nc = EXACT ? NCX : nc_rt;
+  const int nvec = EXACT ? NCX * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;  // float2 pairs per vector
   extern __shared__ __align__(128) unsigned char smem[];
   const int team_threads = (nc + 1) * 32;
@@ -263,25 +263,30 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
 // ---------------------------------------------------------------------------
 namespace {
 
-template <class E, int V>
-void* fwd_kernel_for_v(bool exact) {
-  return exact ? reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, fwd_rows(V), true>)
-               : reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, fwd_rows(V), false>);
+template <class E, int V, int NCX>
+void* fwd_inst() {
+  return reinterpret_cast<void*>(&adaln_fwd_kernel<E, V, fwd_rows(V), NCX>);
 }
 
+// The instantiation for (variant, fixed warp count or 0); compiled_exact lists
+// the fixed counts.
 template <class E>
-void* fwd_kernel_for(int variant, bool exact) {
+void* fwd_kernel_for(int variant, int ncx) {
   switch (variant) {
-    case 5: return fwd_kernel_for_v<E, 5>(exact);
-    case 1: return fwd_kernel_for_v<E, 1>(exact);
-    case 4: return fwd_kernel_for_v<E, 4>(exact);
-    case 2: return fwd_kernel_for_v<E, 2>(exact);
-    default: return fwd_kernel_for_v<E, 3>(exact);
+    case 5: return ncx == 1 ? fwd_inst<E, 5, 1>() : ncx == 2 ? fwd_inst<E, 5, 2>()
+                 : ncx == 3 ? fwd_inst<E, 5, 3>() : fwd_inst<E, 5, 0>();
+    case 1: return fwd_inst<E, 1, 6>();
+    case 4: return ncx == 2 ? fwd_inst<E, 4, 2>() : ncx == 3 ? fwd_inst<E, 4, 3>()
+                 : fwd_inst<E, 4, 0>();
+    case 2: return ncx == 4 ? fwd_inst<E, 2, 4>() : ncx == 5 ? fwd_inst<E, 2, 5>()
+                 : fwd_inst<E, 2, 0>();
+    default: return ncx == 6 ? fwd_inst<E, 3, 6>() : ncx == 8 ? fwd_inst<E, 3, 8>()
+                  : fwd_inst<E, 3, 0>();
   }
 }
 
-void* pick_fwd(adaln_dtype_t dt, int variant, bool exact) {
-  return dt == ADALN_BF16 ? fwd_kernel_for<BF16>(variant, exact) : fwd_kernel_for<F32>(variant, exact);
+void* pick_fwd(adaln_dtype_t dt, int variant, int ncx) {
+  return dt == ADALN_BF16 ? fwd_kernel_for<BF16>(variant, ncx) : fwd_kernel_for<F32>(variant, ncx);
 }
 
 }  // namespace
@@ -299,7 +304,7 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   s->row_bytes = D * esize;
   s->nvec = s->row_bytes / 16;
   s->variant = variant;
-  s->exact = variant_exact(variant, s->nvec);
+  s->ncx = exact_warps(variant, s->nvec);
   s->vpt = variant_vpt(s->variant);
   s->nc = (s->nvec + 32 * s->vpt - 1) / (32 * s->vpt);
   // The kernel is compiled for `teams` teams of the variant's largest warp
@@ -375,7 +380,7 @@ cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
   const int v = choose_variant(nvec);
-  return staging_shape(pick_fwd(dt, v, variant_exact(v, nvec)), T, D, dt, 1, fwd_rows(v), v,
+  return staging_shape(pick_fwd(dt, v, exact_warps(v, nvec)), T, D, dt, 1, fwd_rows(v), v,
                        variant_min_blocks(v), kCtaHeaderBytes, s);
 }
 
@@ -441,7 +446,7 @@ int64_t device_rows_plan(const FwdArgs& a, const Shape& s, int R) {
 
 cudaError_t launch_fwd(const FwdArgs& a, adaln_dtype_t dt, const Shape& s,
                        cudaStream_t st) {
-  void* k = pick_fwd(dt, s.variant, s.exact);
+  void* k = pick_fwd(dt, s.variant, s.ncx);
   int nc = s.nc, stages = s.stages, nvec = s.nvec, team_bytes = s.team_bytes;
   FwdArgs args = a;
   args.ticket = nullptr;

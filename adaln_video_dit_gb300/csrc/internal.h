@@ -68,14 +68,29 @@ ADALN_HD constexpr int variant_max_threads(int v) { return (variant_max_warps(v)
 // takes 4 for short rows, 2 otherwise (two tensors per stage).
 ADALN_HD constexpr int fwd_rows(int v) { return (void)v, 4; }
 ADALN_HD constexpr int bwd_rows(int v) { return v == 6 ? 4 : 2; }
-// The row fills the variant's largest consumer-warp count exactly.
-ADALN_HD inline bool variant_exact(int v, int nvec) {
-  return nvec == variant_max_warps(v) * 32 * variant_vpt(v);
+// Consumer-warp counts with a compiled fixed-width instantiation per variant
+// (forward and backward alike; variant 1 serves the forward only at 6): the
+// variant's largest count and the counts of the common power-of-two widths
+// (bf16 D = 512, 1024, 2048, 4096, 6144; fp32 half those).
+ADALN_HD constexpr bool compiled_exact(int v, int nc) {
+  return v == 5 || v == 6 ? (nc >= 1 && nc <= 3)
+         : v == 1         ? nc == 6
+         : v == 4         ? (nc == 2 || nc == 3)
+         : v == 2         ? (nc == 4 || nc == 5)
+                          : (nc == 6 || nc == 8);
+}
+// The fixed-width instantiation for a row of nvec vectors: its consumer-warp
+// count when the row fills that many warps exactly and it is compiled, else
+// 0 (the generic instantiation, warp count and row length at run time).
+ADALN_HD inline int exact_warps(int v, int nvec) {
+  const int per_warp = 32 * variant_vpt(v);
+  const int nc = nvec / per_warp;
+  return nc * per_warp == nvec && compiled_exact(v, nc) ? nc : 0;
 }
 
 struct Shape {
   int variant;    // compiled variant (choose_variant)
-  bool exact;     // nvec fills the variant's largest warp count exactly
+  int ncx;        // fixed-width instantiation's warp count (exact_warps), or 0
   int vpt;        // 16-byte vectors per thread per row (1, 2 or 4)
   int nc;         // consumer warps of a team
   int teams;      // teams per CTA (a team: nc consumer warps + a producer warp)
