@@ -56,11 +56,13 @@ def parse_args():
                         "block x 30 blocks), each its own shift/scale, back to back")
     p.add_argument("--graph", action="store_true",
                    help="with --sites: replay each step as one captured CUDA graph")
-    p.add_argument("--report", choices=["unfused", "shapes", "fixed-cost"], default=None,
+    p.add_argument("--report", choices=["unfused", "shapes", "fixed-cost", "widths"],
+                   default=None,
                    help="instead of the benchmark line: compare with torch's unfused "
                         "chain (time and saved activation bytes), shape-benchmark the "
-                        "operator and fit the step-time cost model, or split a call's "
-                        "fixed cost into host and GPU time")
+                        "operator and fit the step-time cost model, split a call's "
+                        "fixed cost into host and GPU time, or time the forward and "
+                        "backward over a grid of row widths of both dtypes")
     return p.parse_args()
 
 
@@ -775,6 +777,81 @@ def report_shapes(args):
         "b_shape": {str(k): v for k, v in buckets.items()}}))
 
 
+def report_widths(args):
+    """Forward and backward per call over a grid of row widths D (bf16 and
+    fp32, T = 32768 rows in 4 segments, seeded synthetic inputs): median of 30
+    calls, L2 evicted before every call, algorithmic GB/s as a fraction of the
+    measured copy peak, and the launch shape each width gets."""
+    import statistics
+    import torch
+    from adaln_video_dit_gb300 import _lib as L
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, device=dev)
+    fo = torch.empty((), device=dev)
+    peak, peak_kind = peaks()
+    T, nseg = 32768, 4
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(17)
+    rows = []
+    for dt, widths in ((torch.bfloat16, (512, 1024, 1536, 2048, 3072, 4096, 5120, 6144, 8192)),
+                       (torch.float32, (512, 1024, 1536, 2048, 3072, 4096))):
+        es = 2 if dt == torch.bfloat16 else 4
+        for D in widths:
+            x = torch.randn(T, D, device=dev, generator=gen).to(dt)
+            dy = (torch.randn(T, D, device=dev, generator=gen) * 1e-2).to(dt)
+            sh = (torch.randn(nseg, D, device=dev, generator=gen) * 0.5).to(dt)
+            sc = (torch.randn(nseg, D, device=dev, generator=gen) * 0.5).to(dt)
+            seg = (torch.arange(T, device=dev) * nseg // T).to(torch.int32)
+            y, dx = torch.empty_like(x), torch.empty_like(x)
+            mean, rstd = torch.empty(T, device=dev), torch.empty(T, device=dev)
+            dsh, dsc = torch.empty(nseg, D, device=dev), torch.empty(nseg, D, device=dev)
+            ws = torch.empty(L.adaln_bwd_workspace_size(T, D, nseg, dt), device=dev,
+                             dtype=torch.uint8)
+
+            def fwd():
+                L.adaln_fwd(x, sh, sc, seg, 1e-6, y=y, mean=mean, rstd=rstd)
+
+            def bwd():
+                L.adaln_bwd(dy, x, mean, rstd, sc, seg, dx=dx, dshift=dsh, dscale=dsc,
+                            workspace=ws)
+
+            for _ in range(3):
+                fwd()
+                bwd()
+            tf, tb = [], []
+            for _ in range(30):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                torch.sum(flush, dim=0, out=fo)
+                ev[0].record()
+                fwd()
+                ev[1].record()
+                torch.sum(flush, dim=0, out=fo)
+                ev[2].record()
+                bwd()
+                ev[3].record()
+                torch.cuda.synchronize()
+                tf.append(ev[0].elapsed_time(ev[1]) * 1e3)
+                tb.append(ev[2].elapsed_time(ev[3]) * 1e3)
+            rc, bits = L.adaln_get_status()
+            if rc != L.ADALN_OK:
+                raise RuntimeError(f"device status: {L.strerror(rc)} ({bits})")
+            ab = alg_bytes(T, D, nseg, es)
+            mf, mb = statistics.median(tf), statistics.median(tb)
+            rows.append({
+                "dtype": "bf16" if es == 2 else "f32", "D": D,
+                "fwd_us": round(mf, 1), "fwd_frac": round(ab["fwd"] / (mf * 1e3) / peak, 3),
+                "bwd_us": round(mb, 1), "bwd_frac": round(ab["bwd"] / (mb * 1e3) / peak, 3),
+                "fwd_shape": L.adaln_launch_shape(L.ADALN_KERNEL_FWD, T, D, nseg, dt),
+                "bwd_shape": L.adaln_launch_shape(L.ADALN_KERNEL_BWD_ROWS, T, D, nseg, dt)})
+            del x, dy, y, dx, ws
+    print(json.dumps({"report": "widths", "device": torch.cuda.get_device_name(0), "T": T,
+                      "nseg": nseg, "peak_gbs": peak, "peak_kind": peak_kind,
+                      "l2": "evicted before every call", "rows": rows}))
+
+
 def report_fixed_cost(args):
     """Where a call's time goes, host or GPU, per workload: host time of one
     call through the C ABI (the raw ctypes call and the Python binding with
@@ -994,6 +1071,9 @@ def main():
         return
     if args.report == "fixed-cost":
         report_fixed_cost(args)
+        return
+    if args.report == "widths":
+        report_widths(args)
         return
     rank, local, world, pg = dist_setup(args.gpus)
     if args.sites > 1 and args.impl == "native":
