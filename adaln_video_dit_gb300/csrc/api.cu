@@ -32,21 +32,27 @@ int check_dims(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dt) {
   return ADALN_OK;
 }
 
-// ----- launch-shape cache, keyed by (device, kernel, dtype, D) -------------
+// ----- launch-shape cache, keyed by (device, kernel, variant, dtype, D) ------
 struct ShapeKey {
-  int dev, which, dt, D;
+  int dev, which, variant, dt, D;
   bool operator==(const ShapeKey& o) const {
-    return dev == o.dev && which == o.which && dt == o.dt && D == o.D;
+    return dev == o.dev && which == o.which && variant == o.variant && dt == o.dt && D == o.D;
   }
 };
 std::mutex g_shape_mu;
 std::vector<std::pair<ShapeKey, Shape>> g_shapes;
 
-cudaError_t get_shape(int which, int64_t T, int32_t D, adaln_dtype_t dt, Shape* out) {
+// seg_rows: rows per segment of the whole batch (the forward's variant
+// choice; a call on a chunk of a batch passes the batch's).
+cudaError_t get_shape(int which, int64_t T, int32_t D, int64_t seg_rows, adaln_dtype_t dt,
+                      Shape* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const ShapeKey key{dev, which, (int)dt, D};
+  const int nvec = D * (dt == ADALN_BF16 ? 2 : 4) / 16;
+  const int variant = which == ADALN_KERNEL_FWD ? choose_fwd_variant(nvec, seg_rows)
+                                                : choose_bwd_variant(nvec);
+  const ShapeKey key{dev, which, variant, (int)dt, D};
   Shape full{};
   bool found = false;
   {
@@ -57,7 +63,8 @@ cudaError_t get_shape(int which, int64_t T, int32_t D, adaln_dtype_t dt, Shape* 
   if (!found) {
     // Computed with an unbounded T: grid = SMs x resident CTAs per SM.
     const int64_t big = (int64_t)1 << 40;
-    e = which == ADALN_KERNEL_FWD ? fwd_shape(big, D, dt, &full) : bwd_shape(big, D, dt, &full);
+    e = which == ADALN_KERNEL_FWD ? fwd_shape(big, D, dt, variant, &full)
+                                  : bwd_shape(big, D, dt, &full);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_shape_mu);
     g_shapes.push_back({key, full});
@@ -204,10 +211,10 @@ cudaError_t launch_slot_release(int pool, int slot, cudaStream_t st, bool launch
 
 int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* seg_id,
             int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, float eps, void* y,
-            float* mean, float* rstd, cudaStream_t st) {
+            float* mean, float* rstd, cudaStream_t st, int64_t seg_rows) {
   if (T == 0) return ADALN_OK;
   Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_FWD, T, D, dtype, &s);
+  cudaError_t e = get_shape(ADALN_KERNEL_FWD, T, D, seg_rows, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
   unsigned* status = nullptr;
   e = status_ptr(&status);
@@ -223,7 +230,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
             adaln_dtype_t dtype, void* dx, float* dshift, float* dscale, void* workspace,
             size_t workspace_bytes, cudaStream_t st, int accumulate) {
   Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
+  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, 0, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
   const size_t need = bwd_workspace_bytes(s, D, nseg);
   if (workspace_bytes < need) return ADALN_ERR_WORKSPACE;
@@ -248,7 +255,7 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
 
 size_t bwd_workspace_need(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, int* rc) {
   Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
+  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, 0, dtype, &s);
   if (e != cudaSuccess) {
     *rc = cuda_fail(e);
     return 0;
@@ -278,7 +285,7 @@ int adaln_fwd(const void* x, const void* shift, const void* scale,
     return ADALN_ERR_ALIGN;
   if (!std::isfinite(eps) || eps < 0.0f) return ADALN_ERR_ARG;
   return adaln::run_fwd(x, shift, scale, seg_id, T, D, nseg, dtype, eps, y, mean, rstd,
-                        static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream), T / nseg);
 }
 
 int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype,
@@ -287,7 +294,7 @@ int adaln_bwd_workspace_size(int64_t T, int32_t D, int32_t nseg, adaln_dtype_t d
   if (rc != ADALN_OK) return rc;
   if (!bytes) return ADALN_ERR_NULL;
   Shape s;
-  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, dtype, &s);
+  cudaError_t e = get_shape(ADALN_KERNEL_BWD_ROWS, T, D, 0, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
   const size_t need = bwd_workspace_bytes(s, D, nseg);
   *bytes = (need + 255) & ~(size_t)255;
@@ -423,7 +430,7 @@ int adaln_launch_shape(int which, int64_t T, int32_t D, int32_t nseg, adaln_dtyp
   if (rc != ADALN_OK) return rc;
   if (which != ADALN_KERNEL_FWD && which != ADALN_KERNEL_BWD_ROWS) return ADALN_ERR_ARG;
   Shape s;
-  cudaError_t e = get_shape(which, T, D, dtype, &s);
+  cudaError_t e = get_shape(which, T, D, T / nseg, dtype, &s);
   if (e != cudaSuccess) return cuda_fail(e);
   if (grid) *grid = s.grid;
   if (threads) *threads = s.threads;

@@ -376,10 +376,9 @@ cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
   return cudaSuccess;
 }
 
-cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s) {
+cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, int v, Shape* s) {
   const int esize = dt == ADALN_BF16 ? 2 : 4;
   const int nvec = D * esize / 16;
-  const int v = choose_variant(nvec);
   return staging_shape(pick_fwd(dt, v, exact_warps(v, nvec)), T, D, dt, 1, fwd_rows(v), v,
                        variant_min_blocks(v), kCtaHeaderBytes, s);
 }

@@ -241,7 +241,7 @@ extern "C" int adaln_fwd_bwd_host(const void* x, const void* dy, const void* shi
     // Compute: forward, then the backward of the chunk, its sums added in order.
     ADALN_CK(cudaStreamWaitEvent(cx->comp, cx->in[sl], 0));
     rc = run_fwd(S + L.x, base + L.shift, base + L.scale, d_seg + r0, rows, D, nseg, dtype, eps,
-                 S + L.y, d_mean + r0, d_rstd + r0, cx->comp);
+                 S + L.y, d_mean + r0, d_rstd + r0, cx->comp, T / nseg);
     if (rc != ADALN_OK) return rc;
     rc = run_bwd(S + L.dy, S + L.x, d_mean + r0, d_rstd + r0, base + L.scale, d_seg + r0, rows,
                  D, nseg, dtype, S + L.dx, d_dshift, d_dscale, base + L.ws, L.ws_bytes,

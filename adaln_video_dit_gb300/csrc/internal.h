@@ -51,6 +51,16 @@ constexpr int kCtaHeaderBytes = 128;
 ADALN_HD inline int choose_variant(int nvec) {
   return nvec <= 192 ? 5 : (nvec < 384 ? 4 : (nvec == 384 ? 1 : (nvec <= 640 ? 2 : 3)));
 }
+// The forward of 384 vectors (D = 3072 bf16, 1536 fp32) has two compiled
+// shapes: variant 1 (two teams of 6 warps) and variant 4 (three teams of 3
+// warps, 4 vectors a thread).  Variant 4 is faster when segments are long
+// (T = 36864 in 16 segments, the MMDiT joint layer: 73.7 vs 77.8 us; every
+// T from 8192 to 262144 with 2300 or more rows a segment: 2-15 % faster)
+// and slower when they are short (about 640 rows: 6-8 % slower from
+// T = 65536 on), so it takes the rows per segment into account.
+ADALN_HD inline int choose_fwd_variant(int nvec, int64_t rows_per_segment) {
+  return nvec == 384 && rows_per_segment >= 1024 ? 4 : choose_variant(nvec);
+}
 ADALN_HD inline int choose_bwd_variant(int nvec) {
   return nvec <= 192 ? 6 : (nvec <= 384 ? 4 : (nvec <= 640 ? 2 : 3));
 }
@@ -149,7 +159,7 @@ struct BwdArgs {
 
 // Launch shapes (depend on the current device).  Return cudaSuccess or the
 // error of the device query.
-cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s);
+cudaError_t fwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, int variant, Shape* s);
 cudaError_t bwd_shape(int64_t T, int32_t D, adaln_dtype_t dt, Shape* s);
 
 // Number of fp32 partial slots of the backward: G + nseg - 1.
@@ -195,10 +205,12 @@ cudaError_t launch_bwd_finalize(const BwdArgs& a, const Shape& s,
 
 // Launch parts of the C entry points (api.cu), without argument checks; the
 // backward can add its sums into dshift/dscale (accumulate = 1) for callers
-// that process the rows in chunks.
+// that process the rows in chunks, and the forward takes the rows per
+// segment of the whole batch (seg_rows: its variant choice, so that a chunk
+// computes what the whole call would).
 int run_fwd(const void* x, const void* shift, const void* scale, const int32_t* seg_id,
             int64_t T, int32_t D, int32_t nseg, adaln_dtype_t dtype, float eps, void* y,
-            float* mean, float* rstd, cudaStream_t st);
+            float* mean, float* rstd, cudaStream_t st, int64_t seg_rows);
 int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
             const void* scale, const int32_t* seg_id, int64_t T, int32_t D, int32_t nseg,
             adaln_dtype_t dtype, void* dx, float* dshift, float* dscale, void* workspace,

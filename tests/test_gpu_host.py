@@ -27,6 +27,8 @@ CASES = [
     (300, 1536, 2, "bf16", [120, 180], 1000),  # one chunk, T below the chunk size
     (2049, 512, 3, "f32", [0, 2049, 0], 256),  # fp32, empty first/last segments
     (0, 256, 2, "bf16", [0, 0], 64),           # no rows: gradients are zero
+    (6000, 3072, 2, "bf16", None, 1000),     # the forward's shape follows the batch's
+                                             # rows per segment, not a chunk's
 ]
 
 

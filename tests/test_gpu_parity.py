@@ -260,6 +260,12 @@ def test_launch_shape_matches_the_rules(adaln):
     for which in (adaln.ADALN_KERNEL_FWD, adaln.ADALN_KERNEL_BWD_ROWS):
         s = adaln.adaln_launch_shape(which, 32768, 2048, 4, torch.bfloat16)
         assert s["threads"] == 4 * 3 * 32 and s["grid"] == sms
+    # D = 3072 bf16 (384 vectors): the forward runs three teams of 3 + 1 warps
+    # when segments are long, two of 6 + 1 when they are short.
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 36864, 3072, 16, torch.bfloat16)
+    assert s["threads"] == 3 * 4 * 32
+    s = adaln.adaln_launch_shape(adaln.ADALN_KERNEL_FWD, 36864, 3072, 64, torch.bfloat16)
+    assert s["threads"] == 2 * 7 * 32
 
 
 def test_cuda_graph_capture_matches_eager(adaln):
