@@ -73,10 +73,10 @@ __device__ __forceinline__ void flush_partials(float* partials, int64_t slot, in
 // registers) and the flush of the run's partial between runs.  A chunk that
 // a segment boundary splits is visited once per run, each visit handling its
 // rows of that run; its stage is released after the last visit.
-// EXACT: the row fills the variant's largest consumer-warp count exactly
-// (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
-// the warp count and row length are compile-time constants (offsets fold
-// into immediates, no per-vector guards).
+// NCX: 0 for the generic instantiation (warp count and row length at run
+// time), else a consumer-warp count the row fills exactly (nvec = NCX x 32 x
+// VPT; the counts compiled_exact lists), which makes both compile-time
+// constants (offsets fold into immediates, no per-vector guards).
 //
 // A CTA holds `teams` teams (one per SM share of the variant); team k of CTA c
 // owns the contiguous row range of virtual CTA v = c * teams + k, so the

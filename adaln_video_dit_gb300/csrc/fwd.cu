@@ -30,10 +30,10 @@ namespace adaln {
 // CTAs share the first rows in contiguous ranges and all teams share a
 // device-wide tail (a.tail_rows).  Every row's result is independent of
 // which team computes it.
-// EXACT: the row fills the variant's largest consumer-warp count exactly
-// (nvec = max warps x 32 x VPT: D = 1536, 3072, 5120, 8192 in bf16), so
-// the warp count and row length are compile-time constants (offsets fold
-// into immediates, no per-vector guards).
+// NCX: 0 for the generic instantiation (warp count and row length at run
+// time), else a consumer-warp count the row fills exactly (nvec = NCX x 32 x
+// VPT; the counts compiled_exact lists), which makes both compile-time
+// constants (offsets fold into immediates, no per-vector guards).
 template <class E, int VARIANT, int R, int NCX>
 __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_threads(VARIANT), 1)
     adaln_fwd_kernel(FwdArgs a, int nc_rt, int stages, int nvec_rt, int team_bytes) {
@@ -292,11 +292,11 @@ void* pick_fwd(adaln_dtype_t dt, int variant, int ncx) {
 }  // namespace
 
 // Common shape rule of the staging kernels: the compiled variant for the row
-// length, consumer warps to cover the row, `teams` teams per CTA after a
-// `cta_header`-byte CTA header, ring depth
-// sized for about 160 KB of staged rows per SM over the teams the variant is
-// sized for (variant_min_blocks per SM), and persistent CTAs = SMs x resident
-// CTAs per SM (at most T).
+// length, consumer warps to cover the row, `teams` teams per CTA (the
+// variant's count, or more when smaller teams fit its thread budget) after a
+// `cta_header`-byte CTA header, ring depth sized for about 160 KB of staged
+// rows per SM over those teams, and persistent CTAs = SMs x resident CTAs per
+// SM (at most T).
 cudaError_t staging_shape(void* kernel, int64_t T, int32_t D, adaln_dtype_t dt,
                           int ntensors, int rows_per_round, int variant, int teams,
                           int cta_header, Shape* s) {
