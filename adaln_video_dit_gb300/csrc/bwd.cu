@@ -92,9 +92,6 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   const int nvec = EXACT ? NCX * 32 * VPT : nvec_rt;
   constexpr int H = E::EPV / 2;
   extern __shared__ __align__(128) unsigned char smem[];
-  // Let the finalize grid be scheduled as soon as SMs free up; it waits for
-  // this grid's completion before reading anything.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int team_threads = (nc + 1) * 32;
   const int teams = blockDim.x / team_threads;
   const int team = threadIdx.x / team_threads;
@@ -104,8 +101,11 @@ __global__ void __launch_bounds__(variant_min_blocks(VARIANT) * variant_max_thre
   __syncthreads();
   // Launched as a programmatic dependent of the stream's previous kernel
   // (typically the forward that wrote mean and rstd): nothing in global
-  // memory is read before that kernel has completed.
+  // memory is read before that kernel has completed.  Only then may the
+  // finalize be scheduled (as SMs free up): it reads seg_id before waiting
+  // for this grid, so every kernel before this one must have completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int64_t G = (int64_t)gridDim.x * teams;  // virtual CTAs
   const int64_t v = (int64_t)blockIdx.x * teams + team;

@@ -44,10 +44,10 @@ constexpr int kCtaHeaderBytes = 128;
 //   variant 4: nvec <=  384  VPT 4, <= 3 warps, 3 teams (backward: its column
 //              sums favour few warps per row, many rows per SM; forward below
 //              384 vectors, where 2-warp teams fit four to an SM)
-// A row that needs fewer warps than the variant's largest count runs more,
-// smaller teams in the same thread budget (staging_shape).
 //   variant 2: nvec <=  640  VPT 4, <= 5 warps, 2 teams
 //   variant 3: nvec <= 1024  VPT 4, <= 8 warps, 1 team
+// A row that needs fewer warps than the variant's largest count runs more,
+// smaller teams in the same thread budget (staging_shape).
 ADALN_HD inline int choose_variant(int nvec) {
   return nvec <= 192 ? 5 : (nvec < 384 ? 4 : (nvec == 384 ? 1 : (nvec <= 640 ? 2 : 3)));
 }

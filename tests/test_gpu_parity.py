@@ -304,16 +304,19 @@ def test_cuda_graph_capture_matches_eager(adaln):
 
 
 
-def test_inputs_written_by_the_previous_kernel_are_read_after_it(adaln):
+@pytest.mark.parametrize("T,D,nseg", [(20000, 3072, 3), (300, 1024, 5)])
+def test_inputs_written_by_the_previous_kernel_are_read_after_it(adaln, T, D, nseg):
     """The row kernels are launched as programmatic dependents of the
     stream's previous kernel: inputs that a torch kernel writes just before
     each call (no synchronisation in between) must be read only after it
-    has completed.  The buffers hold other data until those kernels run."""
-    c = I.random_case(77, 20000, 3072, 3, dtype="bf16")
+    has completed, seg_id included (the finalize reads it before waiting for
+    the row pass; with few rows it has SMs to itself early).  The buffers
+    hold other, valid data until those kernels run."""
+    c = I.random_case(77 + T, T, D, nseg, dtype="bf16")
     d = H.device_inputs(c)
-    T, D, nseg = c["T"], c["D"], c["nseg"]
     x = torch.full_like(d["x"], 7.0)
     dy = torch.full_like(d["dy"], -3.0)
+    seg = torch.zeros_like(d["seg_id"])  # every row in segment 0
     y = torch.empty_like(x)
     mean = torch.empty(T, device="cuda")
     rstd = torch.empty(T, device="cuda")
@@ -321,8 +324,9 @@ def test_inputs_written_by_the_previous_kernel_are_read_after_it(adaln):
     torch.cuda._sleep(int(2e6))  # keep the GPU busy so the launches queue up
     x.copy_(d["x"])              # the previous kernel writes x ...
     adaln.adaln_fwd(x, d["shift"], d["scale"], d["seg_id"], c["eps"], y=y, mean=mean, rstd=rstd)
-    dy.copy_(d["dy"])            # ... and dy
-    dx, dsh, dsc = adaln.adaln_bwd(dy, x, mean, rstd, d["scale"], d["seg_id"])
+    dy.copy_(d["dy"])            # ... dy
+    seg.copy_(d["seg_id"])       # ... and seg_id
+    dx, dsh, dsc = adaln.adaln_bwd(dy, x, mean, rstd, d["scale"], seg)
     torch.cuda.synchronize()
     H.check_against_oracle(c, d, dict(y=y, mean=mean, rstd=rstd, dx=dx, dshift=dsh, dscale=dsc))
 
